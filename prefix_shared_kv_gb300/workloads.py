@@ -1,0 +1,394 @@
+"""Seeded synthetic inputs for prefix-shared KV attention.
+
+This module only draws numbers and lays out index tables: Q/K/V values (fp32 N(0,1) rounded to
+bf16, round-to-nearest-even), the random order in which pool slots are handed out, token ids and
+request lengths.  It holds none of the method's arithmetic, so the fp64 oracle and the CUDA path
+can both be fed from it without sharing any code that computes attention.
+
+Workload shapes follow the pages' workloads:
+
+* a shared system prompt followed by short per-user questions (prefix-caching comparison page,
+  section on the 1,000-token common prefix and the 40-token question);
+* shared prefixes of 2,000 and 16,000 tokens at sharing degree 16 (BatchLLM explainer, Global
+  Prefix Sharing and the micro-benchmark table);
+* a three-level radix tree (system prompt -> branches -> leaves) as in the RadixAttention tree
+  figures of the SGLang explainer.
+
+Every pool is "page size 1": each token owns one slot of ``[pool_size, num_kv_heads, head_dim]``
+and slots are handed out in a random permutation, so neighbouring tokens never sit in
+neighbouring slots.  Token ids of cached runs are drawn from [0, 16000) and those of new runs from
+[16000, 32000), so a new token can never extend a cached match by chance.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+from typing import List, Optional, Sequence
+
+import numpy as np
+
+HEAD_DIM = 128
+CACHED_TOKEN_RANGE = (0, 16000)
+NEW_TOKEN_RANGE = (16000, 32000)
+
+
+def bf16_bits(x: np.ndarray) -> np.ndarray:
+    """fp32 array -> bf16 bit patterns (uint16), round-to-nearest-even (inputs are finite)."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    b = x.view(np.uint32)
+    out = np.empty(x.shape, dtype=np.uint16)
+    flat_b = b.reshape(-1)
+    flat_o = out.reshape(-1)
+    step = 1 << 24
+    for s in range(0, flat_b.size, step):
+        bb = flat_b[s:s + step]
+        flat_o[s:s + step] = ((bb + (0x7FFF + ((bb >> 16) & 1))) >> 16).astype(np.uint16)
+    return out
+
+
+def normal_bf16(rng: np.random.Generator, shape) -> np.ndarray:
+    return bf16_bits(rng.standard_normal(shape, dtype=np.float32))
+
+
+@dataclass
+class Run:
+    """A run of consecutive token positions and the pool slots holding their KV."""
+    slots: np.ndarray            # int32 [n]
+    tokens: np.ndarray           # int32 [n]
+    cached: bool                 # True: KV already in the pool; False: stored during the step
+    k: Optional[np.ndarray] = None   # uint16 [n, Hkv, d] for new runs
+    v: Optional[np.ndarray] = None
+
+    def __len__(self) -> int:
+        return int(self.slots.shape[0])
+
+
+@dataclass
+class ExtendBatch:
+    req_idx: np.ndarray          # int32 [B]   row of req_to_token for each request
+    prefix_len: np.ndarray       # int32 [B]   cached tokens before the new ones
+    extend_len: np.ndarray       # int32 [B]   new tokens
+    cu_q: np.ndarray             # int32 [B+1] row offsets of each request in q/o
+    q: np.ndarray                # uint16 [sum(extend_len), Hq, d]
+    group_of_req: np.ndarray     # int32 [B]   -1 = no declared shared prefix
+    group_prefix_len: np.ndarray  # int32 [G]
+    tokens: List[np.ndarray] = field(default_factory=list)  # full token ids per request
+
+
+@dataclass
+class DecodeBatch:
+    req_idx: np.ndarray          # int32 [B]
+    seq_len: np.ndarray          # int32 [B]   keys 0..seq_len-1, the current token included
+    q: np.ndarray                # uint16 [B, Hq, d]
+    group_of_req: np.ndarray     # int32 [B]
+    group_prefix_len: np.ndarray  # int32 [G]
+
+
+@dataclass
+class Step:
+    store_slots: np.ndarray      # int32 [T]
+    k_new: np.ndarray            # uint16 [T, Hkv, d]
+    v_new: np.ndarray
+    extend: Optional[ExtendBatch] = None
+    decode: Optional[DecodeBatch] = None
+
+
+@dataclass
+class Workload:
+    name: str
+    num_q_heads: int
+    num_kv_heads: int
+    head_dim: int
+    softmax_scale: float
+    pool_size: int
+    req_to_token: np.ndarray     # int32 [R, W]
+    k_pool: np.ndarray           # uint16 [P, Hkv, d], cached KV present, all else zero
+    v_pool: np.ndarray
+    steps: List[Step]
+    cached_sequences: List[tuple] = field(default_factory=list)  # (tokens, slots) held by a cache
+    recipe: str = ""
+
+
+class Builder:
+    """Allocates runs in a randomly permuted page-1 pool and assembles req_to_token rows."""
+
+    def __init__(self, rng: np.random.Generator, num_q_heads: int, num_kv_heads: int,
+                 pool_size: int, head_dim: int = HEAD_DIM):
+        self.rng = rng
+        self.hq, self.hkv, self.d = num_q_heads, num_kv_heads, head_dim
+        self.pool_size = pool_size
+        self.perm = rng.permutation(pool_size).astype(np.int32)
+        self.next = 0
+        self.k_pool = np.zeros((pool_size, num_kv_heads, head_dim), dtype=np.uint16)
+        self.v_pool = np.zeros((pool_size, num_kv_heads, head_dim), dtype=np.uint16)
+        self.rows: List[np.ndarray] = []
+
+    def _alloc(self, n: int) -> np.ndarray:
+        if self.next + n > self.pool_size:
+            raise ValueError(f"pool of {self.pool_size} slots exhausted")
+        s = self.perm[self.next:self.next + n].copy()
+        self.next += n
+        return s
+
+    def cached(self, n: int) -> Run:
+        slots = self._alloc(n)
+        tokens = self.rng.integers(*CACHED_TOKEN_RANGE, size=n).astype(np.int32)
+        shape = (n, self.hkv, self.d)
+        self.k_pool[slots] = normal_bf16(self.rng, shape)
+        self.v_pool[slots] = normal_bf16(self.rng, shape)
+        return Run(slots, tokens, True)
+
+    def new(self, n: int) -> Run:
+        slots = self._alloc(n)
+        tokens = self.rng.integers(*NEW_TOKEN_RANGE, size=n).astype(np.int32)
+        shape = (n, self.hkv, self.d)
+        return Run(slots, tokens, False, normal_bf16(self.rng, shape), normal_bf16(self.rng, shape))
+
+    def row(self, runs: Sequence[Run]) -> int:
+        self.rows.append(np.concatenate([r.slots for r in runs]).astype(np.int32)
+                         if runs else np.zeros(0, np.int32))
+        return len(self.rows) - 1
+
+    def q(self, n_rows: int) -> np.ndarray:
+        return normal_bf16(self.rng, (n_rows, self.hq, self.d))
+
+    def finish(self, name: str, steps_spec, cached_sequences, recipe: str) -> Workload:
+        """steps_spec: list of (new_runs, extend_spec, decode_spec) with row ids; rows are then
+        placed at randomly permuted req_to_token indices."""
+        n_rows = len(self.rows)
+        width = max([len(r) for r in self.rows] + [1])
+        width = (width + 15) // 16 * 16
+        row_perm = self.rng.permutation(n_rows).astype(np.int32)
+        r2t = np.zeros((n_rows, width), dtype=np.int32)
+        for i, r in enumerate(self.rows):
+            r2t[row_perm[i], :len(r)] = r
+        steps = []
+        for new_runs, ext, dec in steps_spec:
+            if new_runs:
+                slots = np.concatenate([r.slots for r in new_runs]).astype(np.int32)
+                kn = np.concatenate([r.k for r in new_runs])
+                vn = np.concatenate([r.v for r in new_runs])
+            else:
+                slots = np.zeros(0, np.int32)
+                kn = np.zeros((0, self.hkv, self.d), np.uint16)
+                vn = kn.copy()
+            e = d = None
+            if ext is not None:
+                rows, pl, el, grp, gpl, toks = ext
+                el = np.asarray(el, np.int32)
+                cu = np.zeros(len(el) + 1, np.int32)
+                cu[1:] = np.cumsum(el)
+                e = ExtendBatch(row_perm[np.asarray(rows, np.int64)].astype(np.int32),
+                                np.asarray(pl, np.int32), el, cu, self.q(int(cu[-1])),
+                                np.asarray(grp, np.int32), np.asarray(gpl, np.int32), toks)
+            if dec is not None:
+                rows, sl, grp, gpl = dec
+                d = DecodeBatch(row_perm[np.asarray(rows, np.int64)].astype(np.int32),
+                                np.asarray(sl, np.int32), self.q(len(rows)),
+                                np.asarray(grp, np.int32), np.asarray(gpl, np.int32))
+            steps.append(Step(slots, kn, vn, e, d))
+        return Workload(name, self.hq, self.hkv, self.d, 1.0 / float(np.sqrt(self.d)),
+                        self.pool_size, r2t, self.k_pool, self.v_pool, steps,
+                        cached_sequences, recipe)
+
+
+def _tokens(runs: Sequence[Run]) -> np.ndarray:
+    return np.concatenate([r.tokens for r in runs]).astype(np.int32)
+
+
+def _slots(runs: Sequence[Run]) -> np.ndarray:
+    return np.concatenate([r.slots for r in runs]).astype(np.int32)
+
+
+# --------------------------------------------------------------------------------------------
+# Generic shapes used by the named workloads and by the parity tests.
+# --------------------------------------------------------------------------------------------
+
+def extend_workload(seed: int, num_q_heads: int, num_kv_heads: int, *, n_groups: int,
+                    members: int, prefix: int, ext_lo: int, ext_hi: int,
+                    own_cached_hi: int = 0, ungrouped: int = 0, ungrouped_prefix: int = 0,
+                    pool_size: Optional[int] = None, name: str = "extend") -> Workload:
+    """Groups of `members` requests share a cached `prefix`; each request may also hold
+    U[0, own_cached_hi] cached tokens of its own, then extends U[ext_lo, ext_hi] new tokens.
+    `ungrouped` more requests have their own cached prefix of `ungrouped_prefix` tokens."""
+    rng = np.random.default_rng(seed)
+    n_req = n_groups * members + ungrouped
+    ext = rng.integers(ext_lo, ext_hi + 1, size=n_req)
+    own = rng.integers(0, own_cached_hi + 1, size=n_req) if own_cached_hi > 0 else np.zeros(n_req, np.int64)
+    need = n_groups * prefix + int(ext.sum()) + int(own.sum()) + ungrouped * ungrouped_prefix
+    P = pool_size if pool_size is not None else max(4096, 1 << int(np.ceil(np.log2(need * 1.25))))
+    b = Builder(rng, num_q_heads, num_kv_heads, P)
+    rows, pl, grp, toks, new_runs, cached_seqs = [], [], [], [], [], []
+    gpl = []
+    i = 0
+    for g in range(n_groups):
+        pre = b.cached(prefix) if prefix > 0 else None
+        gpl.append(prefix)
+        if pre is not None:
+            cached_seqs.append((pre.tokens.copy(), pre.slots.copy()))
+        for _ in range(members):
+            runs = [pre] if pre is not None else []
+            if own[i] > 0:
+                runs.append(b.cached(int(own[i])))
+                cached_seqs.append((_tokens(runs), _slots(runs)))
+            nr = b.new(int(ext[i]))
+            new_runs.append(nr)
+            rows.append(b.row(runs + [nr]))
+            pl.append(sum(len(r) for r in runs))
+            grp.append(g)
+            toks.append(_tokens(runs + [nr]))
+            i += 1
+    for _ in range(ungrouped):
+        runs = [b.cached(ungrouped_prefix)] if ungrouped_prefix > 0 else []
+        if runs:
+            cached_seqs.append((_tokens(runs), _slots(runs)))
+        nr = b.new(int(ext[i]))
+        new_runs.append(nr)
+        rows.append(b.row(runs + [nr]))
+        pl.append(ungrouped_prefix)
+        grp.append(-1)
+        toks.append(_tokens(runs + [nr]))
+        i += 1
+    recipe = (f"seed {seed}; Hq={num_q_heads} Hkv={num_kv_heads} d=128; {n_groups} groups x "
+              f"{members} requests on a cached {prefix}-token prefix; own cached U[0,{own_cached_hi}];"
+              f" new U[{ext_lo},{ext_hi}]; {ungrouped} ungrouped (prefix {ungrouped_prefix});"
+              f" pool {P} slots, random permutation")
+    return b.finish(name, [(new_runs, (rows, pl, [len(r) for r in new_runs], grp, gpl, toks), None)],
+                    cached_seqs, recipe)
+
+
+def decode_workload(seed: int, num_q_heads: int, num_kv_heads: int, *, n_groups: int,
+                    members: int, prefix: int, dist_lo: int, dist_hi: int,
+                    ungrouped: int = 0, min_pool: int = 0, name: str = "decode") -> Workload:
+    """Groups of `members` requests share a cached `prefix`; each request holds U[dist_lo,
+    dist_hi] distinct tokens of which the last is the current token (stored in the step).
+    `ungrouped` more requests hold only distinct tokens."""
+    rng = np.random.default_rng(seed)
+    n_req = n_groups * members + ungrouped
+    dist = rng.integers(dist_lo, dist_hi + 1, size=n_req)
+    need = n_groups * prefix + int(dist.sum())
+    P = max(min_pool, need) if min_pool else max(4096, 1 << int(np.ceil(np.log2(need * 1.25))))
+    b = Builder(rng, num_q_heads, num_kv_heads, P)
+    rows, sl, grp, gpl, new_runs, cached_seqs = [], [], [], [], [], []
+    i = 0
+    for g in range(n_groups):
+        pre = b.cached(prefix) if prefix > 0 else None
+        gpl.append(prefix)
+        if pre is not None:
+            cached_seqs.append((pre.tokens.copy(), pre.slots.copy()))
+        for _ in range(members):
+            runs = [pre] if pre is not None else []
+            if dist[i] > 1:
+                runs.append(b.cached(int(dist[i]) - 1))
+            cur = b.new(1)
+            new_runs.append(cur)
+            rows.append(b.row(runs + [cur]))
+            sl.append(prefix + int(dist[i]))
+            grp.append(g)
+            i += 1
+    for _ in range(ungrouped):
+        runs = [b.cached(int(dist[i]) - 1)] if dist[i] > 1 else []
+        cur = b.new(1)
+        new_runs.append(cur)
+        rows.append(b.row(runs + [cur]))
+        sl.append(int(dist[i]))
+        grp.append(-1)
+        i += 1
+    recipe = (f"seed {seed}; Hq={num_q_heads} Hkv={num_kv_heads} d=128; {n_groups} groups x "
+              f"{members} requests on a cached {prefix}-token prefix; distinct U[{dist_lo},{dist_hi}]"
+              f" incl. the current token; {ungrouped} ungrouped; pool {P} slots, random permutation")
+    return b.finish(name, [(new_runs, None, (rows, sl, grp, gpl))], cached_seqs, recipe)
+
+
+# --------------------------------------------------------------------------------------------
+# The five named workloads.
+# --------------------------------------------------------------------------------------------
+
+def tiny(seed: int = 1001) -> Workload:
+    """8 q / 2 kv heads; one cached 1000-token prefix in a 4096-slot pool; 4 requests extend 40
+    new tokens each (causal), then 8 decode steps of one token per request."""
+    rng = np.random.default_rng(seed)
+    b = Builder(rng, 8, 2, 4096)
+    pre = b.cached(1000)
+    ext = [b.new(40) for _ in range(4)]
+    dec = [[b.new(1) for _ in range(8)] for _ in range(4)]
+    rows = [b.row([pre, ext[i]] + dec[i]) for i in range(4)]
+    toks = [_tokens([pre, ext[i]]) for i in range(4)]
+    steps = [(ext, (rows, [1000] * 4, [40] * 4, [0] * 4, [1000], toks), None)]
+    for s in range(8):
+        steps.append(([dec[i][s] for i in range(4)], None,
+                      (rows, [1041 + s] * 4, [0] * 4, [1000])))
+    return b.finish("tiny-8q2kv-p1000", steps, [(pre.tokens.copy(), pre.slots.copy())],
+                    f"seed {seed}; Hq=8 Hkv=2 d=128; cached prefix 1000; 4 x 40 extend; "
+                    f"8 decode steps; pool 4096 slots, random permutation")
+
+
+def llama7b_extend(seed: int = 1002) -> Workload:
+    """32/32 heads; 4 groups x 16 requests on a cached 2000-token prefix; each extends U[40,200]."""
+    return extend_workload(seed, 32, 32, n_groups=4, members=16, prefix=2000, ext_lo=40,
+                           ext_hi=200, pool_size=32768, name="llama7b-extend-4x16-p2000")
+
+
+def llama7b_decode_hf(seed: int = 1003) -> Workload:
+    """32/32 heads; 16 groups x 16 requests on a 2000-token prefix; distinct U[100,500]."""
+    return decode_workload(seed, 32, 32, n_groups=16, members=16, prefix=2000, dist_lo=100,
+                           dist_hi=500, name="llama7b-decode-16x16-p2000")
+
+
+def llama3_gqa_decode(seed: int = 1004) -> Workload:
+    """32 q / 8 kv heads; 16 groups x 16 requests on a 16000-token prefix; distinct U[200,1000];
+    pool of at least 409,600 slots."""
+    return decode_workload(seed, 32, 8, n_groups=16, members=16, prefix=16000, dist_lo=200,
+                           dist_hi=1000, min_pool=409600, name="llama3-gqa-decode-16x16-p16000")
+
+
+def radix_mixed(seed: int = 1005) -> Workload:
+    """Radix tree 1000 -> 8 x 500 -> 4 x 200 per branch (32 leaves).  One step: 16 leaf requests
+    extend 64 tokens; 8 cache misses run a 1500-token full prefill; 40 decode requests, request j on
+    leaf j mod 32 with its own tail of U[1,32] tokens (the last one current)."""
+    rng = np.random.default_rng(seed)
+    tails = rng.integers(1, 33, size=40)
+    b = Builder(rng, 32, 32, 32768)
+    sysp = b.cached(1000)
+    branch = [b.cached(500) for _ in range(8)]
+    leaf = [b.cached(200) for _ in range(32)]
+    paths = [[sysp, branch[k // 4], leaf[k]] for k in range(32)]
+    cached_seqs = [(_tokens(p), _slots(p)) for p in paths]
+    new_runs, e_rows, e_pl, e_el, e_grp, e_toks = [], [], [], [], [], []
+    for k in range(16):
+        nr = b.new(64)
+        new_runs.append(nr)
+        e_rows.append(b.row(paths[k] + [nr]))
+        e_pl.append(1700); e_el.append(64); e_grp.append(0)
+        e_toks.append(_tokens(paths[k] + [nr]))
+    for _ in range(8):
+        nr = b.new(1500)
+        new_runs.append(nr)
+        e_rows.append(b.row([nr]))
+        e_pl.append(0); e_el.append(1500); e_grp.append(-1)
+        e_toks.append(nr.tokens.copy())
+    d_rows, d_sl = [], []
+    for j in range(40):
+        runs = list(paths[j % 32])
+        if tails[j] > 1:
+            tail = b.cached(int(tails[j]) - 1)
+            runs.append(tail)
+            cached_seqs.append((_tokens(runs), _slots(runs)))
+        cur = b.new(1)
+        new_runs.append(cur)
+        d_rows.append(b.row(runs + [cur]))
+        d_sl.append(1700 + int(tails[j]))
+    step = (new_runs, (e_rows, e_pl, e_el, e_grp, [1000], e_toks),
+            (d_rows, d_sl, [0] * 40, [1000]))
+    return b.finish("radix-mixed-1000-8x500-32x200", [step], cached_seqs,
+                    f"seed {seed}; Hq=Hkv=32 d=128; tree 1000 -> 8x500 -> 32x200; 16 extend "
+                    f"(p=1700, E=64) + 8 miss (p=0, E=1500) + 40 decode (tail U[1,32]); "
+                    f"shared-prefix groups at the 1000-token system prompt; pool 32768 slots")
+
+
+NAMED = {
+    "tiny": tiny,
+    "extend": llama7b_extend,
+    "decode": llama7b_decode_hf,
+    "gqa-decode": llama3_gqa_decode,
+    "radix-mixed": radix_mixed,
+}
