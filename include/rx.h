@@ -1,0 +1,192 @@
+/*
+ * rx.h -- prefix-shared KV attention on a page-size-1 KV pool, for sm_103a (GB300).
+ *
+ * The operations follow the pages' statement of the problem:
+ *   - the KV cache is held on the GPU in pages of ONE token, and each cached token sequence refers
+ *     to the pages of its tokens (SGLang explainer "論文解説: SGLang - RadixAttention...",
+ *     section RadixAttention; LMSYS blog translation, RadixAttention backend);
+ *   - a new request reuses the KV of its longest cached prefix and computes only the unmatched
+ *     tokens (same explainer, "主要な操作: プレフィックスマッチング");
+ *   - requests that share a prefix attend to the shared-prefix KV and to their own KV in one
+ *     kernel, different thread blocks taking the two parts (BatchLLM explainer
+ *     "論文解説: BatchLLM - ...", section Horizontal Fusion).
+ *
+ * Conventions for every call
+ * --------------------------
+ *  Memory   All tensors are caller-owned.  Pointers marked (device) are CUDA device memory,
+ *           (host) are ordinary host memory.  The library keeps no device allocation between
+ *           calls; scratch ("workspace") is sized by the library and passed in by the caller.
+ *  Layout   bf16 tensors, row-major, 16-byte aligned:
+ *             K pool, V pool   [pool_size, num_kv_heads, head_dim]   slot-major (page = 1 token)
+ *             q, o             [rows, num_q_heads, head_dim]
+ *             lse              [rows, num_q_heads] float32, natural log of sum_j exp(s_j)
+ *             req_to_token     [rows_of_table, stride] int32: entry (r, j) is the pool slot of
+ *                              key position j of the request stored in table row r.
+ *  Heads    query head h reads KV head h / (num_q_heads / num_kv_heads).
+ *  Shapes   head_dim must be 128; num_q_heads / num_kv_heads in {1, 2, 4, 8}.
+ *  Streams  Device work is enqueued on `stream` (a cudaStream_t, NULL = legacy default stream)
+ *           and is asynchronous; calls return RX_OK once it is enqueued.
+ *  Errors   Argument checks run on the host before anything is enqueued; a failed check returns
+ *           its code and enqueues nothing.  rx_last_error() gives a message for the calling
+ *           thread's last failure.  Kernels never trap and never wait without a bound: a device
+ *           wait that runs out records RX_ERR_TIMEOUT in the workspace status word, read back with
+ *           rx_read_status().
+ */
+#ifndef RX_H_
+#define RX_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  RX_OK = 0,
+  RX_ERR_INVALID = 1,      /* bad pointer, alignment, negative length, inconsistent plan */
+  RX_ERR_RANGE = 2,        /* a length or index exceeds the table, pool or plan limits */
+  RX_ERR_UNSUPPORTED = 3,  /* head_dim != 128, head ratio outside {1,2,4,8} */
+  RX_ERR_CUDA = 4,         /* a CUDA runtime call failed (see rx_last_error) */
+  RX_ERR_TIMEOUT = 5,      /* a bounded device wait ran out (reported by rx_read_status) */
+  RX_ERR_WORKSPACE = 6     /* workspace missing or smaller than the plan needs */
+} rx_status;
+
+typedef void* rx_stream_t; /* a cudaStream_t */
+
+const char* rx_status_string(int status);
+const char* rx_last_error(void);
+
+/* Shape of the KV pool and of the request -> slot table. */
+typedef struct {
+  int32_t num_q_heads;
+  int32_t num_kv_heads;
+  int32_t head_dim;             /* must be 128 */
+  float softmax_scale;          /* scores are softmax_scale * q.k */
+  int64_t pool_size;            /* slots in each of the K and V pools */
+  const int32_t* req_to_token;  /* (device) [req_to_token_rows, req_to_token_stride] */
+  int64_t req_to_token_rows;
+  int64_t req_to_token_stride;  /* elements per table row; every length is <= this */
+} rx_kv_desc;
+
+/* ---------------------------------------------------------------------------------------------
+ * rx_store_kv -- write the KV of new tokens into their pool pages.
+ *
+ * The cache keeps each token's KV in a page of its own (SGLang explainer, RadixAttention: one
+ * token per page); storing a newly computed token is a scatter into its slot:
+ *   k_pool[slots[t]] = k_new[t],  v_pool[slots[t]] = v_new[t]   for t < num_tokens.
+ *   k_new, v_new (device) [num_tokens, num_kv_heads, head_dim] bf16; slots (device) int32.
+ * Bit-exact copy.  Slots must be distinct and in [0, pool_size); a slot outside that range is
+ * skipped by the kernel (nothing is written for that token).  Duplicate slots leave one of the
+ * writers' rows (unspecified which).  num_tokens == 0 is a no-op.
+ * ------------------------------------------------------------------------------------------- */
+rx_status rx_store_kv(const rx_kv_desc* desc, void* k_pool, void* v_pool, const void* k_new,
+                      const void* v_new, const int32_t* slots, int64_t num_tokens,
+                      rx_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------------
+ * Plans.  Attention work is split into work items on the host from host copies of the lengths
+ * (the radix-tree match that produces them runs on the CPU as well: SGLang explainer, RadixAttention
+ * -- the tree is kept on the CPU).  A plan is built once per batch, uploaded into the caller's
+ * device workspace once, and can then drive any number of attention calls (e.g. every layer)
+ * with the same lengths.
+ * ------------------------------------------------------------------------------------------- */
+typedef struct rx_plan rx_plan;
+
+rx_status rx_plan_create(rx_plan** out);
+void rx_plan_destroy(rx_plan* plan);
+/* Bytes of device workspace the built plan needs (tables + partial results). */
+rx_status rx_plan_workspace_size(const rx_plan* plan, size_t* bytes);
+/* Copy the plan's tables into `workspace` (device, >= rx_plan_workspace_size bytes, 256-byte
+ * aligned) with cudaMemcpyAsync on `stream`.  The plan object may be rebuilt or destroyed as soon
+ * as this returns. */
+rx_status rx_plan_upload(const rx_plan* plan, void* workspace, size_t workspace_bytes,
+                         rx_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------------
+ * rx_extend_plan / rx_extend_attn -- attention of new tokens over their cached prefix plus causal
+ * attention among themselves (prefill with a radix-cache hit: only the unmatched part is computed;
+ * SGLang explainer, prefix matching; SGLang paper notes App. A.1).
+ *
+ * Request r (r < batch) owns table row req_idx[r]; its key positions 0..prefix_len[r]-1 are
+ * cached and positions prefix_len[r]..prefix_len[r]+extend_len[r]-1 are its new tokens, whose KV
+ * must already be stored (rx_store_kv).  Its new rows sit in q/o/lse at rows
+ * cu[r]..cu[r]+extend_len[r]-1, cu = exclusive prefix sum of extend_len (requests packed in batch
+ * order).  New row i attends to key positions 0..prefix_len[r]+i:
+ *   o = softmax_j(scale * q.k_j) v_j,   lse = log sum_j exp(scale * q.k_j).
+ * Shared prefixes: group_of_req[r] = g >= 0 declares that the first group_prefix_len[g] entries of
+ * row req_idx[r] equal those of every other member of g (g < num_groups, group_prefix_len[g] <=
+ * prefix_len[r]); the kernel then reads that prefix KV once for all new rows of the group.  -1 (or
+ * group_of_req == NULL) declares no sharing.  The result does not depend on the grouping.
+ * All arrays of rx_extend_plan are (host).  extend_len[r] == 0 is allowed; sum of extend_len must
+ * be < 2^31.
+ * ------------------------------------------------------------------------------------------- */
+rx_status rx_extend_plan(rx_plan* plan, const rx_kv_desc* desc, int32_t batch,
+                         const int32_t* req_idx, const int32_t* prefix_len,
+                         const int32_t* extend_len, const int32_t* group_of_req,
+                         int32_t num_groups, const int32_t* group_prefix_len);
+rx_status rx_extend_attn(const rx_plan* plan, const rx_kv_desc* desc, const void* k_pool,
+                         const void* v_pool, const void* q, void* o, float* lse,
+                         void* workspace, size_t workspace_bytes, rx_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------------
+ * rx_decode_plan / rx_decode_attn -- one query token per request over all of its keys, the current
+ * token included (the caller stores it first).  Request b owns table row req_idx[b] and attends to
+ * key positions 0..seq_len[b]-1; q/o rows are b, lse row b.
+ * Horizontal fusion (BatchLLM explainer, Horizontal Fusion): for a group g (group_of_req[b] = g),
+ * the first group_prefix_len[g] keys -- equal in every member's row -- are read from HBM once and
+ * scored against all members' queries; each member's remaining keys are read by other thread
+ * blocks of the same launch, and the partial softmax states are combined by a log-sum-exp merge.
+ * seq_len[b] >= 1 and >= group_prefix_len[group_of_req[b]].  Arrays of rx_decode_plan are (host).
+ * ------------------------------------------------------------------------------------------- */
+rx_status rx_decode_plan(rx_plan* plan, const rx_kv_desc* desc, int32_t batch,
+                         const int32_t* req_idx, const int32_t* seq_len,
+                         const int32_t* group_of_req, int32_t num_groups,
+                         const int32_t* group_prefix_len);
+rx_status rx_decode_attn(const rx_plan* plan, const rx_kv_desc* desc, const void* k_pool,
+                         const void* v_pool, const void* q, void* o, float* lse,
+                         void* workspace, size_t workspace_bytes, rx_stream_t stream);
+
+/* Read (synchronously, on `stream`) and clear the device status word of a workspace that a plan
+ * was uploaded to.  *status receives RX_OK or the first device-side error recorded. */
+rx_status rx_read_status(const void* workspace, int32_t* status, rx_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------------
+ * Host radix cache: token sequences -> pool slots, edges labelled with token runs (SGLang
+ * explainer, RadixAttention: radix tree whose nodes refer to the pages of their tokens).
+ * All arguments (host).  Not thread-safe per object.
+ * ------------------------------------------------------------------------------------------- */
+typedef struct rx_radix rx_radix;
+
+rx_status rx_radix_create(rx_radix** out);
+void rx_radix_destroy(rx_radix* tree);
+/* Insert tokens[0..n) whose KV sits in slots[0..n).  Tokens already cached keep their existing
+ * slots (the caller's slots for them are not referenced); *new_tokens (nullable) receives how
+ * many tokens were added.  A partially matched edge is split. */
+rx_status rx_radix_insert(rx_radix* tree, const int32_t* tokens, const int32_t* slots, int64_t n,
+                          int64_t* new_tokens);
+/* Longest cached prefix of tokens[0..n), floored to match_unit (>= 1): the tokens a prefill can
+ * skip (prefix-caching comparison page: 992 of a 1,000-token prefix at unit 16, 1,000 at unit 1).
+ * out_slots (nullable, capacity n) receives the slots of the saved tokens. */
+rx_status rx_radix_match(const rx_radix* tree, const int32_t* tokens, int64_t n,
+                         int32_t match_unit, int64_t* saved, int32_t* out_slots);
+/* Number of tokens (= pool slots) the tree holds, and its node count (root excluded). */
+rx_status rx_radix_stats(const rx_radix* tree, int64_t* tokens, int64_t* nodes);
+
+/* ---------------------------------------------------------------------------------------------
+ * Token accounting (host, pure functions).
+ * ------------------------------------------------------------------------------------------- */
+/* Tokens a prefill skips when `matched` leading tokens hit at match unit `unit`: floor to unit. */
+int64_t rx_saved_tokens(int64_t matched, int32_t unit);
+/* BatchLLM token-saving ratio, percent: (1 - n_processed / n_logical) * 100 (BatchLLM explainer,
+ * Global Prefix Sharing, Equation 2).  Returns NaN if n_logical <= 0. */
+double rx_token_saving(int64_t n_processed, int64_t n_logical);
+/* Compute removed by a hit: l_prefix / (l_prefix + l_new) (SGLang explainer, RadixAttention,
+ * Reduction formula).  NaN if the sum is 0. */
+double rx_compute_reduction(int64_t l_prefix, int64_t l_new);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RX_H_ */

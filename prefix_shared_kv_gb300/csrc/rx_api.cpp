@@ -1,0 +1,537 @@
+// C-ABI of the library: argument checks, the host work planners, the radix cache and the token
+// accounting.  Device work is in the .cu files; this file launches nothing itself.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <limits>
+#include <memory>
+#include <numeric>
+#include <string>
+#include <unordered_map>
+#include <vector>
+
+#include "rx_internal.h"
+
+using namespace rx;
+
+namespace {
+
+thread_local std::string g_err;
+
+rx_status fail(rx_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return st;
+}
+
+rx_status cuda_fail(int e, const char* what) {
+  return fail(RX_ERR_CUDA, "%s: %s", what, cudaGetErrorString((cudaError_t)e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+rx_status check_desc(const rx_kv_desc* d, bool need_table) {
+  if (!d) return fail(RX_ERR_INVALID, "desc is NULL");
+  if (d->head_dim != kHeadDim) return fail(RX_ERR_UNSUPPORTED, "head_dim %d != 128", d->head_dim);
+  if (d->num_kv_heads <= 0 || d->num_q_heads <= 0)
+    return fail(RX_ERR_INVALID, "head counts must be positive");
+  if (d->num_q_heads % d->num_kv_heads)
+    return fail(RX_ERR_UNSUPPORTED, "num_q_heads %% num_kv_heads != 0");
+  const int gq = d->num_q_heads / d->num_kv_heads;
+  if (gq != 1 && gq != 2 && gq != 4 && gq != 8)
+    return fail(RX_ERR_UNSUPPORTED, "head ratio %d not in {1,2,4,8}", gq);
+  if (d->num_kv_heads > 256) return fail(RX_ERR_UNSUPPORTED, "num_kv_heads > 256");
+  if (d->pool_size <= 0 || d->pool_size > (int64_t)INT32_MAX)
+    return fail(RX_ERR_INVALID, "pool_size must be in [1, 2^31)");
+  if (!(d->softmax_scale > 0.f) || !std::isfinite(d->softmax_scale))
+    return fail(RX_ERR_INVALID, "softmax_scale must be finite and > 0");
+  if (need_table) {
+    if (!d->req_to_token) return fail(RX_ERR_INVALID, "req_to_token is NULL");
+    if (d->req_to_token_rows <= 0 || d->req_to_token_stride <= 0 ||
+        d->req_to_token_stride > (int64_t)INT32_MAX || d->req_to_token_rows > (int64_t)INT32_MAX)
+      return fail(RX_ERR_INVALID, "bad req_to_token shape");
+  }
+  return RX_OK;
+}
+
+int device_sms() {
+  static int cached = 0;
+  if (cached) return cached;
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess &&
+      cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && n > 0) {
+    cached = n;
+  } else {
+    cudaGetLastError();
+    n = 152;
+  }
+  return n;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+}  // namespace
+
+// ---------------------------------------------------------------------------------------------
+// Plans
+// ---------------------------------------------------------------------------------------------
+struct rx_plan {
+  int kind = 0;  // 0 = empty, 1 = extend, 2 = decode
+  std::vector<uint8_t> blob;  // header + tables, uploaded verbatim
+  size_t ws_bytes = 0;
+  int32_t hq = 0, hkv = 0;
+  int64_t rows = 0, stride = 0, pool = 0;
+  const int32_t* table = nullptr;
+  PlanHeader hdr() const {
+    PlanHeader h;
+    std::memcpy(&h, blob.data(), sizeof h);
+    return h;
+  }
+};
+
+namespace {
+
+template <typename T>
+void put(std::vector<uint8_t>& blob, int64_t off, const std::vector<T>& v) {
+  if (!v.empty()) std::memcpy(blob.data() + off, v.data(), v.size() * sizeof(T));
+}
+
+void remember_desc(rx_plan* p, const rx_kv_desc* d) {
+  p->hq = d->num_q_heads;
+  p->hkv = d->num_kv_heads;
+  p->rows = d->req_to_token_rows;
+  p->stride = d->req_to_token_stride;
+  p->pool = d->pool_size;
+  p->table = d->req_to_token;
+}
+
+rx_status check_plan_use(const rx_plan* p, int kind, const rx_kv_desc* d, const void* k,
+                         const void* v, const void* q, const void* o, const void* lse,
+                         const void* ws, size_t ws_bytes) {
+  if (!p) return fail(RX_ERR_INVALID, "plan is NULL");
+  if (p->kind != kind)
+    return fail(RX_ERR_INVALID, "plan was built for %s", p->kind == 1 ? "extend" : p->kind == 2 ? "decode" : "nothing");
+  rx_status st = check_desc(d, true);
+  if (st) return st;
+  if (d->num_q_heads != p->hq || d->num_kv_heads != p->hkv || d->req_to_token_rows != p->rows ||
+      d->req_to_token_stride != p->stride || d->pool_size != p->pool)
+    return fail(RX_ERR_INVALID, "descriptor differs from the one the plan was built with");
+  const PlanHeader h = p->hdr();
+  if (h.n_items > 0 || h.batch > 0) {
+    if (!k || !v || !q || !o || !lse) return fail(RX_ERR_INVALID, "NULL tensor pointer");
+    if (!aligned16(k) || !aligned16(v) || !aligned16(q) || !aligned16(o) || !aligned16(lse))
+      return fail(RX_ERR_INVALID, "tensors must be 16-byte aligned");
+  }
+  if (!ws) return fail(RX_ERR_WORKSPACE, "workspace is NULL");
+  if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0)
+    return fail(RX_ERR_INVALID, "workspace must be 256-byte aligned");
+  if (ws_bytes < p->ws_bytes)
+    return fail(RX_ERR_WORKSPACE, "workspace of %zu bytes < %zu needed", ws_bytes, p->ws_bytes);
+  return RX_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* rx_status_string(int s) {
+  switch (s) {
+    case RX_OK: return "ok";
+    case RX_ERR_INVALID: return "invalid argument";
+    case RX_ERR_RANGE: return "out of range";
+    case RX_ERR_UNSUPPORTED: return "unsupported shape";
+    case RX_ERR_CUDA: return "CUDA error";
+    case RX_ERR_TIMEOUT: return "device wait timed out";
+    case RX_ERR_WORKSPACE: return "workspace too small";
+    default: return "unknown status";
+  }
+}
+
+const char* rx_last_error(void) { return g_err.c_str(); }
+
+rx_status rx_store_kv(const rx_kv_desc* desc, void* k_pool, void* v_pool, const void* k_new,
+                      const void* v_new, const int32_t* slots, int64_t num_tokens,
+                      rx_stream_t stream) {
+  rx_status st = check_desc(desc, false);
+  if (st) return st;
+  if (num_tokens < 0) return fail(RX_ERR_INVALID, "num_tokens < 0");
+  if (num_tokens == 0) return RX_OK;
+  if (!k_pool || !v_pool || !k_new || !v_new || !slots)
+    return fail(RX_ERR_INVALID, "NULL pointer");
+  if (!aligned16(k_pool) || !aligned16(v_pool) || !aligned16(k_new) || !aligned16(v_new))
+    return fail(RX_ERR_INVALID, "K/V pointers must be 16-byte aligned");
+  if (num_tokens > (int64_t)INT32_MAX) return fail(RX_ERR_RANGE, "num_tokens >= 2^31");
+  const int e = launch_store_kv(desc, k_pool, v_pool, k_new, v_new, slots, num_tokens, stream);
+  return e ? cuda_fail(e, "store_kv launch") : RX_OK;
+}
+
+rx_status rx_plan_create(rx_plan** out) {
+  if (!out) return fail(RX_ERR_INVALID, "out is NULL");
+  *out = new rx_plan();
+  return RX_OK;
+}
+
+void rx_plan_destroy(rx_plan* plan) { delete plan; }
+
+rx_status rx_plan_workspace_size(const rx_plan* plan, size_t* bytes) {
+  if (!plan || !bytes) return fail(RX_ERR_INVALID, "NULL argument");
+  if (!plan->kind) return fail(RX_ERR_INVALID, "plan has not been built");
+  *bytes = plan->ws_bytes;
+  return RX_OK;
+}
+
+rx_status rx_plan_upload(const rx_plan* plan, void* workspace, size_t workspace_bytes,
+                         rx_stream_t stream) {
+  if (!plan || !plan->kind) return fail(RX_ERR_INVALID, "plan has not been built");
+  if (!workspace) return fail(RX_ERR_WORKSPACE, "workspace is NULL");
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return fail(RX_ERR_INVALID, "workspace must be 256-byte aligned");
+  if (workspace_bytes < plan->ws_bytes)
+    return fail(RX_ERR_WORKSPACE, "workspace of %zu bytes < %zu needed", workspace_bytes,
+                plan->ws_bytes);
+  cudaError_t e = cudaMemcpyAsync(workspace, plan->blob.data(), plan->blob.size(),
+                                  cudaMemcpyHostToDevice, (cudaStream_t)stream);
+  return e ? cuda_fail(e, "plan upload") : RX_OK;
+}
+
+// ---------------------------------------------------------------------------------------------
+// Decode planner.  Work units: (group, member tile, prefix chunk) for shared prefixes and
+// (request, own-key chunk) for the rest; each unit becomes one item per KV-head block.  Chunk
+// lengths aim at about three items' worth of bytes per SM so a longest-first launch order
+// balances; partial rows are allocated per unit over all KV heads.
+// ---------------------------------------------------------------------------------------------
+rx_status rx_decode_plan(rx_plan* plan, const rx_kv_desc* desc, int32_t batch,
+                         const int32_t* req_idx, const int32_t* seq_len,
+                         const int32_t* group_of_req, int32_t num_groups,
+                         const int32_t* group_prefix_len) {
+  if (!plan) return fail(RX_ERR_INVALID, "plan is NULL");
+  rx_status st = check_desc(desc, true);
+  if (st) return st;
+  if (batch < 0 || num_groups < 0) return fail(RX_ERR_INVALID, "negative batch or group count");
+  if (batch > 0 && (!req_idx || !seq_len)) return fail(RX_ERR_INVALID, "NULL length array");
+  if (num_groups > 0 && !group_prefix_len) return fail(RX_ERR_INVALID, "group_prefix_len NULL");
+  const int hkv = desc->num_kv_heads, gq = desc->num_q_heads / hkv;
+  std::vector<int> grp(batch, -1);
+  for (int b = 0; b < batch; ++b) {
+    if (req_idx[b] < 0 || req_idx[b] >= desc->req_to_token_rows)
+      return fail(RX_ERR_RANGE, "req_idx[%d] = %d outside the table", b, req_idx[b]);
+    if (seq_len[b] < 1 || seq_len[b] > desc->req_to_token_stride)
+      return fail(RX_ERR_RANGE, "seq_len[%d] = %d outside [1, stride]", b, seq_len[b]);
+    if (group_of_req) {
+      const int g = group_of_req[b];
+      if (g < -1 || g >= num_groups) return fail(RX_ERR_RANGE, "group_of_req[%d] = %d", b, g);
+      if (g >= 0) {
+        if (group_prefix_len[g] < 0 || group_prefix_len[g] > seq_len[b])
+          return fail(RX_ERR_RANGE, "group_prefix_len[%d] = %d exceeds seq_len of member %d", g,
+                      group_prefix_len[g], b);
+        grp[b] = g;
+      }
+    }
+  }
+  std::vector<std::vector<int>> members(num_groups);
+  for (int b = 0; b < batch; ++b)
+    if (grp[b] >= 0) members[grp[b]].push_back(b);
+
+  struct Unit {
+    int kind, kv_row, k_begin, k_end, row_begin, n_tok;
+    int64_t part;
+  };
+  std::vector<Unit> units;
+  std::vector<int32_t> rows;
+  std::vector<std::vector<DecMergeRef>> refs(batch);
+  int64_t npart = 0;
+  const int max_tok = 64 / gq;
+  auto kind_of_rows = [](int r) { return r <= 16 ? 0 : (r <= 32 ? 1 : 2); };
+  auto hb_of = [](int kind) { return kind == 0 ? 8 : (kind == 1 ? 4 : 2); };
+
+  // bytes of K+V per key for one KV head
+  const double key_bytes = 2.0 * kHeadDim * 2;
+  double total = 0;
+  for (int g = 0; g < num_groups; ++g)
+    if (!members[g].empty() && group_prefix_len[g] > 0)
+      total += (double)group_prefix_len[g] * hkv * key_bytes *
+               ((members[g].size() + max_tok - 1) / max_tok);
+  for (int b = 0; b < batch; ++b)
+    total += (double)(seq_len[b] - (grp[b] >= 0 ? group_prefix_len[grp[b]] : 0)) * hkv * key_bytes;
+  const double target = std::min(4.0 * 1048576, std::max(256.0 * 1024, total / (3.0 * device_sms())));
+
+  auto chunks = [&](int len, int kind, std::vector<std::pair<int, int>>& out) {
+    const int hb = std::min(hb_of(kind), hkv);
+    const int nk = 128 / hb_of(kind);
+    int max_keys = (int)(target / (hb * key_bytes));
+    max_keys = std::max(64, std::min(kDecMaxKeysPerItem, max_keys));
+    const int n = (len + max_keys - 1) / max_keys;
+    int c = (len + n - 1) / n;
+    c = (c + nk - 1) / nk * nk;
+    c = std::min(c, kDecMaxKeysPerItem);
+    out.clear();
+    for (int k = 0; k < len; k += c) out.push_back({k, std::min(len, k + c)});
+  };
+  std::vector<std::pair<int, int>> ch;
+
+  for (int g = 0; g < num_groups; ++g) {
+    const int gp = group_prefix_len[g];
+    const auto& mem = members[g];
+    if (mem.empty() || gp == 0) continue;
+    for (size_t t0 = 0; t0 < mem.size(); t0 += max_tok) {
+      const int n_tok = (int)std::min<size_t>(max_tok, mem.size() - t0);
+      const int kind = kind_of_rows(n_tok * gq);
+      const int row_begin = (int)rows.size();
+      for (int i = 0; i < n_tok; ++i) rows.push_back(mem[t0 + i]);
+      chunks(gp, kind, ch);
+      for (auto& c : ch) {
+        const int64_t part = npart;
+        npart += (int64_t)hkv * n_tok * gq;
+        units.push_back({kind, req_idx[mem[t0]], c.first, c.second, row_begin, n_tok, part});
+        for (int i = 0; i < n_tok; ++i)
+          refs[mem[t0 + i]].push_back({(int32_t)part, n_tok * gq, i * gq, 0});
+      }
+    }
+  }
+  for (int b = 0; b < batch; ++b) {
+    const int k0 = grp[b] >= 0 ? group_prefix_len[grp[b]] : 0;
+    if (seq_len[b] <= k0) continue;
+    const int row_begin = (int)rows.size();
+    rows.push_back(b);
+    chunks(seq_len[b] - k0, 0, ch);
+    for (auto& c : ch) {
+      const int64_t part = npart;
+      npart += (int64_t)hkv * gq;
+      units.push_back({0, req_idx[b], k0 + c.first, k0 + c.second, row_begin, 1, part});
+      refs[b].push_back({(int32_t)part, gq, 0, 0});
+    }
+  }
+  if (npart > (int64_t)INT32_MAX) return fail(RX_ERR_RANGE, "plan too large");
+
+  std::vector<DecItem> items;
+  for (const Unit& u : units) {
+    const int hb = hb_of(u.kind);
+    for (int h = 0; h * hb < hkv; ++h)
+      items.push_back({u.kind, h, u.kv_row, u.k_begin, u.k_end, u.row_begin, u.n_tok,
+                       (int32_t)u.part});
+  }
+  auto cost = [&](const DecItem& it) {
+    return (double)(it.k_end - it.k_begin) * std::min(hb_of(it.kind), hkv);
+  };
+  std::stable_sort(items.begin(), items.end(),
+                   [&](const DecItem& a, const DecItem& b) { return cost(a) > cost(b); });
+
+  std::vector<int32_t> midx(batch + 1, 0);
+  std::vector<DecMergeRef> mref;
+  for (int b = 0; b < batch; ++b) {
+    midx[b] = (int32_t)mref.size();
+    mref.insert(mref.end(), refs[b].begin(), refs[b].end());
+  }
+  midx[batch] = (int32_t)mref.size();
+
+  PlanHeader h;
+  std::memset(&h, 0, sizeof h);
+  h.magic = kPlanMagic;
+  h.kind = 2;
+  h.n_items = (int32_t)items.size();
+  h.num_q_heads = desc->num_q_heads;
+  h.num_kv_heads = hkv;
+  h.batch = batch;
+  h.n_rows = (int32_t)rows.size();
+  size_t off = align256(sizeof(PlanHeader));
+  h.off_items = off; off = align256(off + items.size() * sizeof(DecItem));
+  h.off_rows = off; off = align256(off + rows.size() * 4);
+  h.off_segs = off;
+  h.off_merge_idx = off; off = align256(off + midx.size() * 4);
+  h.off_merge = off; off = align256(off + mref.size() * sizeof(DecMergeRef));
+  const size_t tables = off;
+  h.off_part_o = off; off = align256(off + (size_t)npart * kHeadDim * 4);
+  h.off_part_lse = off; off = align256(off + (size_t)npart * 4);
+  h.n_part_rows = npart;
+  h.total_bytes = off;
+  plan->blob.assign(tables, 0);
+  std::memcpy(plan->blob.data(), &h, sizeof h);
+  put(plan->blob, h.off_items, items);
+  put(plan->blob, h.off_rows, rows);
+  put(plan->blob, h.off_merge_idx, midx);
+  put(plan->blob, h.off_merge, mref);
+  plan->ws_bytes = off;
+  plan->kind = 2;
+  remember_desc(plan, desc);
+  return RX_OK;
+}
+
+rx_status rx_decode_attn(const rx_plan* plan, const rx_kv_desc* desc, const void* k_pool,
+                         const void* v_pool, const void* q, void* o, float* lse,
+                         void* workspace, size_t workspace_bytes, rx_stream_t stream) {
+  rx_status st = check_plan_use(plan, 2, desc, k_pool, v_pool, q, o, lse, workspace,
+                                workspace_bytes);
+  if (st) return st;
+  const PlanHeader h = plan->hdr();
+  const int e = launch_decode(desc, &h, k_pool, v_pool, q, o, lse, workspace, stream);
+  return e ? cuda_fail(e, "decode launch") : RX_OK;
+}
+
+// ---------------------------------------------------------------------------------------------
+// Extend planner.  The new tokens of a group's members are packed, member after member, into
+// tiles of 128 / gq tokens (128 query rows per KV head).  A tile's segments: the shared prefix
+// (read from the first member's row, visible to all rows) and, per member present, its keys from
+// the group prefix up to its last row's causal limit.  Ungrouped requests get tiles of their own.
+// One item per (tile, KV head), launched longest first.
+// ---------------------------------------------------------------------------------------------
+rx_status rx_extend_plan(rx_plan* plan, const rx_kv_desc* desc, int32_t batch,
+                         const int32_t* req_idx, const int32_t* prefix_len,
+                         const int32_t* extend_len, const int32_t* group_of_req,
+                         int32_t num_groups, const int32_t* group_prefix_len) {
+  if (!plan) return fail(RX_ERR_INVALID, "plan is NULL");
+  rx_status st = check_desc(desc, true);
+  if (st) return st;
+  if (batch < 0 || num_groups < 0) return fail(RX_ERR_INVALID, "negative batch or group count");
+  if (batch > 0 && (!req_idx || !prefix_len || !extend_len))
+    return fail(RX_ERR_INVALID, "NULL length array");
+  if (num_groups > 0 && !group_prefix_len) return fail(RX_ERR_INVALID, "group_prefix_len NULL");
+  const int hkv = desc->num_kv_heads, gq = desc->num_q_heads / hkv;
+  std::vector<int64_t> cu(batch + 1, 0);
+  std::vector<int> grp(batch, -1);
+  for (int b = 0; b < batch; ++b) {
+    if (req_idx[b] < 0 || req_idx[b] >= desc->req_to_token_rows)
+      return fail(RX_ERR_RANGE, "req_idx[%d] = %d outside the table", b, req_idx[b]);
+    if (prefix_len[b] < 0 || extend_len[b] < 0)
+      return fail(RX_ERR_INVALID, "negative length for request %d", b);
+    if ((int64_t)prefix_len[b] + extend_len[b] > desc->req_to_token_stride)
+      return fail(RX_ERR_RANGE, "prefix_len + extend_len of request %d exceeds the stride", b);
+    cu[b + 1] = cu[b] + extend_len[b];
+    if (group_of_req) {
+      const int g = group_of_req[b];
+      if (g < -1 || g >= num_groups) return fail(RX_ERR_RANGE, "group_of_req[%d] = %d", b, g);
+      if (g >= 0) {
+        if (group_prefix_len[g] < 0 || group_prefix_len[g] > prefix_len[b])
+          return fail(RX_ERR_RANGE, "group_prefix_len[%d] = %d exceeds prefix_len of member %d",
+                      g, group_prefix_len[g], b);
+        grp[b] = g;
+      }
+    }
+  }
+  if (cu[batch] > (int64_t)INT32_MAX) return fail(RX_ERR_RANGE, "sum of extend_len >= 2^31");
+  const int tile_tok = 128 / gq;
+
+  std::vector<ExtRow> rows;
+  std::vector<ExtSeg> segs;
+  struct Tile {
+    int row_begin, n_tok, seg_begin, n_seg;
+    double cost;
+  };
+  std::vector<Tile> tiles;
+
+  auto emit_tiles = [&](const std::vector<int>& reqs, int gp) {
+    // token list of the requests, member after member
+    const int first_row = (int)rows.size();
+    for (int r : reqs)
+      for (int i = 0; i < extend_len[r]; ++i)
+        rows.push_back({(int32_t)(cu[r] + i), prefix_len[r] + i + 1, r, 0});
+    const int n = (int)rows.size() - first_row;
+    for (int t0 = 0; t0 < n; t0 += tile_tok) {
+      const int nt = std::min(tile_tok, n - t0);
+      Tile tl{first_row + t0, nt, (int)segs.size(), 0, 0.0};
+      if (gp > 0) {
+        segs.push_back({req_idx[reqs[0]], 0, gp, -1});
+        tl.cost += (double)gp;
+      }
+      int i = 0;
+      while (i < nt) {
+        const int owner = rows[first_row + t0 + i].owner;
+        int j = i;
+        while (j + 1 < nt && rows[first_row + t0 + j + 1].owner == owner) ++j;
+        const int kend = rows[first_row + t0 + j].kmax;  // last row's causal limit
+        if (kend > gp) {
+          segs.push_back({req_idx[owner], gp, kend, owner});
+          tl.cost += (double)(kend - gp) * (j - i + 1) / nt;
+        }
+        i = j + 1;
+      }
+      tl.n_seg = (int)segs.size() - tl.seg_begin;
+      tiles.push_back(tl);
+    }
+  };
+
+  std::vector<std::vector<int>> members(num_groups);
+  for (int b = 0; b < batch; ++b)
+    if (grp[b] >= 0 && extend_len[b] > 0) members[grp[b]].push_back(b);
+  for (int g = 0; g < num_groups; ++g) {
+    if (members[g].empty()) continue;
+    if (group_prefix_len[g] > 0) {
+      emit_tiles(members[g], group_prefix_len[g]);
+    } else {
+      for (int b : members[g]) emit_tiles(std::vector<int>{b}, 0);
+    }
+  }
+  for (int b = 0; b < batch; ++b)
+    if (grp[b] < 0 && extend_len[b] > 0) emit_tiles(std::vector<int>{b}, 0);
+
+  std::vector<size_t> order(tiles.size());
+  std::iota(order.begin(), order.end(), 0);
+  std::stable_sort(order.begin(), order.end(),
+                   [&](size_t a, size_t b) { return tiles[a].cost > tiles[b].cost; });
+  std::vector<ExtItem> items;
+  items.reserve(tiles.size() * hkv);
+  for (size_t k : order)
+    for (int h = 0; h < hkv; ++h) {
+      const Tile& t = tiles[k];
+      items.push_back({t.row_begin, t.n_tok, t.seg_begin, t.n_seg, h, {0, 0, 0}});
+    }
+  if (items.size() > (size_t)INT32_MAX) return fail(RX_ERR_RANGE, "plan too large");
+
+  PlanHeader h;
+  std::memset(&h, 0, sizeof h);
+  h.magic = kPlanMagic;
+  h.kind = 1;
+  h.n_items = (int32_t)items.size();
+  h.num_q_heads = desc->num_q_heads;
+  h.num_kv_heads = hkv;
+  h.batch = batch;
+  h.n_rows = (int32_t)rows.size();
+  size_t off = align256(sizeof(PlanHeader));
+  h.off_items = off; off = align256(off + items.size() * sizeof(ExtItem));
+  h.off_rows = off; off = align256(off + rows.size() * sizeof(ExtRow));
+  h.off_segs = off; off = align256(off + segs.size() * sizeof(ExtSeg));
+  h.off_merge_idx = h.off_merge = h.off_part_o = h.off_part_lse = off;
+  h.total_bytes = off;
+  plan->blob.assign(off, 0);
+  std::memcpy(plan->blob.data(), &h, sizeof h);
+  put(plan->blob, h.off_items, items);
+  put(plan->blob, h.off_rows, rows);
+  put(plan->blob, h.off_segs, segs);
+  plan->ws_bytes = off;
+  plan->kind = 1;
+  remember_desc(plan, desc);
+  return RX_OK;
+}
+
+rx_status rx_extend_attn(const rx_plan* plan, const rx_kv_desc* desc, const void* k_pool,
+                         const void* v_pool, const void* q, void* o, float* lse,
+                         void* workspace, size_t workspace_bytes, rx_stream_t stream) {
+  rx_status st = check_plan_use(plan, 1, desc, k_pool, v_pool, q, o, lse, workspace,
+                                workspace_bytes);
+  if (st) return st;
+  const PlanHeader h = plan->hdr();
+  const int e = launch_extend(desc, &h, k_pool, v_pool, q, o, lse, workspace, stream);
+  return e ? cuda_fail(e, "extend launch") : RX_OK;
+}
+
+rx_status rx_read_status(const void* workspace, int32_t* status, rx_stream_t stream) {
+  if (!workspace || !status) return fail(RX_ERR_INVALID, "NULL argument");
+  const char* w = static_cast<const char*>(workspace) + offsetof(PlanHeader, status);
+  cudaError_t e = cudaMemcpyAsync(status, w, 4, cudaMemcpyDeviceToHost, (cudaStream_t)stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize((cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "status read");
+  if (*status != 0) {
+    e = cudaMemsetAsync(const_cast<char*>(w), 0, 4, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "status clear");
+  }
+  return RX_OK;
+}
+
+}  // extern "C"

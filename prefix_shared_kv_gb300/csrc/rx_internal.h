@@ -1,0 +1,103 @@
+// Internal tables shared by the host planner (rx_api.cpp) and the kernels (*.cu).
+#pragma once
+#include <stdint.h>
+#include <stddef.h>
+
+#include "rx.h"
+
+namespace rx {
+
+constexpr int kHeadDim = 128;
+constexpr uint32_t kPlanMagic = 0x52585031u;  // "RXP1"
+
+// ---------------------------------------------------------------------------------------------
+// Decode.  A work item reads keys [k_begin, k_end) of one table row, for a block of KV heads, and
+// scores them against up to 64 query rows (n_tok requests x gq query heads per KV head).  Items of
+// a group's shared prefix carry all members (or a tile of them); items of a request's own keys
+// carry that request alone.  Each item leaves normalised partial outputs + base-2 LSE per (KV head,
+// row); the merge pass combines a request's partials.
+// Tilings ("kinds"): warps of a 256-thread CTA map to (KV head in block, 16-row m-tile).
+//   kind 0: 1 m-tile  x 8 heads, 16 keys per stage
+//   kind 1: 2 m-tiles x 4 heads, 32 keys per stage
+//   kind 2: 4 m-tiles x 2 heads, 64 keys per stage
+// Every kind stages 128 (head, key) rows of K and of V per pipeline stage (64 KiB).
+// ---------------------------------------------------------------------------------------------
+struct DecItem {
+  int32_t kind;
+  int32_t head_block;   // KV heads [head_block*HB, head_block*HB + HB)
+  int32_t kv_row;       // req_to_token row giving the slots
+  int32_t k_begin;
+  int32_t k_end;
+  int32_t row_begin;    // first entry in dec_rows (batch indices of the item's requests)
+  int32_t n_tok;        // requests in the item
+  int32_t part;         // partial-row base of the item's work unit (all KV heads)
+};
+
+struct DecMergeRef {    // one partial of a request
+  int32_t part;         // work unit base
+  int32_t rows_real;    // n_tok * gq of that unit
+  int32_t row;          // the request's first row in the unit (token index * gq)
+  int32_t pad;
+};
+
+constexpr int kDecMaxKeysPerItem = 2048;
+constexpr int kDecStages = 3;
+constexpr int kDecStageBytes = 2 * 128 * kHeadDim * 2;   // K + V, 128 rows each
+constexpr size_t kDecSmemBytes = (size_t)kDecStages * kDecStageBytes + kDecMaxKeysPerItem * 4;
+
+// ---------------------------------------------------------------------------------------------
+// Extend.  A work item is a tile of up to 128 query rows (new tokens x gq query heads of one KV
+// head) and a list of key segments.  Segment owner -1 is visible to every row (a shared prefix);
+// owner r is visible only to rows of request r, and only keys at positions < the row's limit.
+// ---------------------------------------------------------------------------------------------
+struct ExtRow {         // one new token
+  int32_t q_row;        // row in q / o / lse
+  int32_t kmax;         // keys at positions >= kmax are masked (prefix_len + i + 1)
+  int32_t owner;        // batch index of the request
+  int32_t pad;
+};
+
+struct ExtSeg {
+  int32_t kv_row;
+  int32_t k_begin;
+  int32_t k_end;
+  int32_t owner;        // -1 = all rows of the item
+};
+
+struct ExtItem {
+  int32_t row_begin;    // into ext_rows
+  int32_t n_tok;        // tokens in the tile (rows = n_tok * gq <= 128)
+  int32_t seg_begin;    // into ext_segs
+  int32_t n_seg;
+  int32_t kv_head;
+  int32_t pad[3];
+};
+
+// Workspace layout written by rx_plan_upload: a 256-byte header, then the tables, then (decode)
+// the partial outputs.  Offsets are in bytes from the workspace base and 256-byte aligned.
+struct PlanHeader {
+  uint32_t magic;
+  int32_t kind;          // 1 = extend, 2 = decode
+  int32_t status;        // device-side error word (rx_status), 0 = OK
+  int32_t n_items;
+  int32_t num_q_heads, num_kv_heads;
+  int32_t batch;
+  int32_t n_rows;        // decode: entries of dec_rows; extend: ext_rows
+  int64_t off_items, off_rows, off_segs, off_merge_idx, off_merge, off_part_o, off_part_lse;
+  int64_t n_part_rows;
+  int64_t total_bytes;
+  int64_t pad[19];
+};
+static_assert(sizeof(PlanHeader) == 256, "header is 256 bytes");
+
+// Launchers (defined in the .cu files).  Return cudaError_t as int.
+int launch_store_kv(const rx_kv_desc* d, void* k_pool, void* v_pool, const void* k_new,
+                    const void* v_new, const int32_t* slots, int64_t n, void* stream);
+int launch_decode(const rx_kv_desc* d, const PlanHeader* h, const void* k_pool,
+                  const void* v_pool, const void* q, void* o, float* lse, void* ws,
+                  void* stream);
+int launch_extend(const rx_kv_desc* d, const PlanHeader* h, const void* k_pool,
+                  const void* v_pool, const void* q, void* o, float* lse, void* ws,
+                  void* stream);
+
+}  // namespace rx

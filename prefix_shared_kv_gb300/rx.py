@@ -1,0 +1,272 @@
+"""Thin Python binding of librx (the C ABI declared in include/rx.h).
+
+Argument marshalling only: every function here forwards to the C entry point of the same name
+(rx_store_kv -> store_kv, ...).  Tensors are torch CUDA tensors (their data_ptr() is passed) and
+the stream defaults to torch's current stream.  There is no fallback: if the library has not been
+built, or a call fails, an exception is raised.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+from typing import Optional
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_lib", "librx.so")
+
+RX_OK, RX_ERR_INVALID, RX_ERR_RANGE, RX_ERR_UNSUPPORTED, RX_ERR_CUDA, RX_ERR_TIMEOUT, \
+    RX_ERR_WORKSPACE = range(7)
+
+EXPORTED = [
+    "rx_status_string", "rx_last_error", "rx_store_kv", "rx_plan_create", "rx_plan_destroy",
+    "rx_plan_workspace_size", "rx_plan_upload", "rx_extend_plan", "rx_extend_attn",
+    "rx_decode_plan", "rx_decode_attn", "rx_read_status", "rx_radix_create", "rx_radix_destroy",
+    "rx_radix_insert", "rx_radix_match", "rx_radix_stats", "rx_saved_tokens", "rx_token_saving",
+    "rx_compute_reduction",
+]
+
+
+class RxError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"{msg} (status {status})")
+        self.status = status
+
+
+class KVDesc(C.Structure):
+    _fields_ = [("num_q_heads", C.c_int32), ("num_kv_heads", C.c_int32),
+                ("head_dim", C.c_int32), ("softmax_scale", C.c_float),
+                ("pool_size", C.c_int64), ("req_to_token", C.c_void_p),
+                ("req_to_token_rows", C.c_int64), ("req_to_token_stride", C.c_int64)]
+
+
+_lib = None
+_P = C.c_void_p
+_I32P = C.POINTER(C.c_int32)
+_I64P = C.POINTER(C.c_int64)
+
+
+def lib():
+    """Load librx.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is not built; run `python -m prefix_shared_kv_gb300.build`")
+    L = C.CDLL(LIB_PATH)
+    sig = {
+        "rx_status_string": (C.c_char_p, [C.c_int]),
+        "rx_last_error": (C.c_char_p, []),
+        "rx_store_kv": (C.c_int, [C.POINTER(KVDesc), _P, _P, _P, _P, _P, C.c_int64, _P]),
+        "rx_plan_create": (C.c_int, [C.POINTER(_P)]),
+        "rx_plan_destroy": (None, [_P]),
+        "rx_plan_workspace_size": (C.c_int, [_P, C.POINTER(C.c_size_t)]),
+        "rx_plan_upload": (C.c_int, [_P, _P, C.c_size_t, _P]),
+        "rx_extend_plan": (C.c_int, [_P, C.POINTER(KVDesc), C.c_int32, _I32P, _I32P, _I32P,
+                                     _I32P, C.c_int32, _I32P]),
+        "rx_extend_attn": (C.c_int, [_P, C.POINTER(KVDesc), _P, _P, _P, _P, _P, _P, C.c_size_t,
+                                     _P]),
+        "rx_decode_plan": (C.c_int, [_P, C.POINTER(KVDesc), C.c_int32, _I32P, _I32P, _I32P,
+                                     C.c_int32, _I32P]),
+        "rx_decode_attn": (C.c_int, [_P, C.POINTER(KVDesc), _P, _P, _P, _P, _P, _P, C.c_size_t,
+                                     _P]),
+        "rx_read_status": (C.c_int, [_P, _I32P, _P]),
+        "rx_radix_create": (C.c_int, [C.POINTER(_P)]),
+        "rx_radix_destroy": (None, [_P]),
+        "rx_radix_insert": (C.c_int, [_P, _I32P, _I32P, C.c_int64, _I64P]),
+        "rx_radix_match": (C.c_int, [_P, _I32P, C.c_int64, C.c_int32, _I64P, _I32P]),
+        "rx_radix_stats": (C.c_int, [_P, _I64P, _I64P]),
+        "rx_saved_tokens": (C.c_int64, [C.c_int64, C.c_int32]),
+        "rx_token_saving": (C.c_double, [C.c_int64, C.c_int64]),
+        "rx_compute_reduction": (C.c_double, [C.c_int64, C.c_int64]),
+    }
+    for name, (res, args) in sig.items():
+        f = getattr(L, name)
+        f.restype = res
+        f.argtypes = args
+    _lib = L
+    return L
+
+
+def _check(status: int):
+    if status != RX_OK:
+        L = lib()
+        raise RxError(status, f"{L.rx_status_string(status).decode()}: {L.rx_last_error().decode()}")
+
+
+def _ptr(t) -> int:
+    if t is None:
+        return 0
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _host_i32(a):
+    """Host int32 array (numpy, list or CPU tensor) -> (numpy array kept alive, pointer)."""
+    if a is None:
+        return None, None
+    if hasattr(a, "cpu") and not isinstance(a, np.ndarray):
+        a = a.cpu().numpy()
+    arr = np.ascontiguousarray(np.asarray(a, dtype=np.int32))
+    return arr, arr.ctypes.data_as(_I32P)
+
+
+def kv_desc(num_q_heads: int, num_kv_heads: int, pool_size: int, req_to_token,
+            softmax_scale: Optional[float] = None, head_dim: int = 128) -> KVDesc:
+    """Descriptor of the pool and of req_to_token (a [rows, stride] int32 CUDA tensor)."""
+    if softmax_scale is None:
+        softmax_scale = head_dim ** -0.5
+    rows, stride = (req_to_token.shape if req_to_token is not None else (0, 0))
+    if req_to_token is not None and req_to_token.stride(1) != 1:
+        raise ValueError("req_to_token rows must be contiguous")
+    return KVDesc(num_q_heads, num_kv_heads, head_dim, softmax_scale, pool_size,
+                  _ptr(req_to_token), rows, req_to_token.stride(0) if req_to_token is not None else 0)
+
+
+def store_kv(desc: KVDesc, k_pool, v_pool, k_new, v_new, slots, stream=None):
+    n = int(slots.shape[0]) if slots is not None else 0
+    _check(lib().rx_store_kv(C.byref(desc), _ptr(k_pool), _ptr(v_pool), _ptr(k_new), _ptr(v_new),
+                             _ptr(slots), n, _stream(stream)))
+
+
+class Plan:
+    """rx_plan: host-built work list for one batch (extend or decode)."""
+
+    def __init__(self):
+        h = _P()
+        _check(lib().rx_plan_create(C.byref(h)))
+        self._h = h
+
+    def close(self):
+        if self._h:
+            lib().rx_plan_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    @property
+    def handle(self):
+        return self._h
+
+    def workspace_size(self) -> int:
+        n = C.c_size_t(0)
+        _check(lib().rx_plan_workspace_size(self._h, C.byref(n)))
+        return n.value
+
+    def upload(self, workspace, nbytes: Optional[int] = None, stream=None):
+        if nbytes is None:
+            nbytes = workspace.numel() * workspace.element_size()
+        _check(lib().rx_plan_upload(self._h, _ptr(workspace), nbytes, _stream(stream)))
+
+
+def extend_plan(plan: Plan, desc: KVDesc, req_idx, prefix_len, extend_len, group_of_req=None,
+                group_prefix_len=None):
+    ri, rip = _host_i32(req_idx)
+    pl, plp = _host_i32(prefix_len)
+    el, elp = _host_i32(extend_len)
+    g, gp_ = _host_i32(group_of_req)
+    gl, glp = _host_i32(group_prefix_len)
+    ng = 0 if gl is None else int(gl.shape[0])
+    _check(lib().rx_extend_plan(plan.handle, C.byref(desc), int(ri.shape[0]), rip, plp, elp, gp_,
+                                ng, glp))
+
+
+def decode_plan(plan: Plan, desc: KVDesc, req_idx, seq_len, group_of_req=None,
+                group_prefix_len=None):
+    ri, rip = _host_i32(req_idx)
+    sl, slp = _host_i32(seq_len)
+    g, gp_ = _host_i32(group_of_req)
+    gl, glp = _host_i32(group_prefix_len)
+    ng = 0 if gl is None else int(gl.shape[0])
+    _check(lib().rx_decode_plan(plan.handle, C.byref(desc), int(ri.shape[0]), rip, slp, gp_, ng,
+                                glp))
+
+
+def _nbytes(t) -> int:
+    if t is None or isinstance(t, int):
+        return 0
+    return t.numel() * t.element_size()
+
+
+def extend_attn(plan: Plan, desc: KVDesc, k_pool, v_pool, q, o, lse, workspace, stream=None):
+    _check(lib().rx_extend_attn(plan.handle, C.byref(desc), _ptr(k_pool), _ptr(v_pool), _ptr(q),
+                                _ptr(o), _ptr(lse), _ptr(workspace), _nbytes(workspace),
+                                _stream(stream)))
+
+
+def decode_attn(plan: Plan, desc: KVDesc, k_pool, v_pool, q, o, lse, workspace, stream=None):
+    _check(lib().rx_decode_attn(plan.handle, C.byref(desc), _ptr(k_pool), _ptr(v_pool), _ptr(q),
+                                _ptr(o), _ptr(lse), _ptr(workspace), _nbytes(workspace),
+                                _stream(stream)))
+
+
+def read_status(workspace, stream=None) -> int:
+    s = C.c_int32(0)
+    _check(lib().rx_read_status(_ptr(workspace), C.byref(s), _stream(stream)))
+    return s.value
+
+
+class Radix:
+    """rx_radix: host radix cache of token sequences -> pool slots."""
+
+    def __init__(self):
+        h = _P()
+        _check(lib().rx_radix_create(C.byref(h)))
+        self._h = h
+
+    def __del__(self):
+        try:
+            if self._h:
+                lib().rx_radix_destroy(self._h)
+                self._h = None
+        except Exception:
+            pass
+
+    def insert(self, tokens, slots) -> int:
+        t, tp = _host_i32(tokens)
+        s, sp = _host_i32(slots)
+        if t.shape != s.shape:
+            raise ValueError("tokens and slots differ in length")
+        n = C.c_int64(0)
+        _check(lib().rx_radix_insert(self._h, tp, sp, int(t.shape[0]), C.byref(n)))
+        return n.value
+
+    def match(self, tokens, match_unit: int = 1, want_slots: bool = True):
+        t, tp = _host_i32(tokens)
+        saved = C.c_int64(0)
+        out = np.zeros(max(1, t.shape[0]), np.int32) if want_slots else None
+        _check(lib().rx_radix_match(self._h, tp, int(t.shape[0]), match_unit, C.byref(saved),
+                                    out.ctypes.data_as(_I32P) if want_slots else None))
+        return (saved.value, out[:saved.value].copy()) if want_slots else saved.value
+
+    def stats(self):
+        a, b = C.c_int64(0), C.c_int64(0)
+        _check(lib().rx_radix_stats(self._h, C.byref(a), C.byref(b)))
+        return a.value, b.value
+
+
+def saved_tokens(matched: int, unit: int) -> int:
+    return lib().rx_saved_tokens(matched, unit)
+
+
+def token_saving(n_processed: int, n_logical: int) -> float:
+    return lib().rx_token_saving(n_processed, n_logical)
+
+
+def compute_reduction(l_prefix: int, l_new: int) -> float:
+    return lib().rx_compute_reduction(l_prefix, l_new)

@@ -1,0 +1,143 @@
+"""Host-side checks of the C ABI (no GPU needed): the library loads and exports every symbol the
+header declares; the radix cache and the accounting agree with the oracle and the pages' values;
+argument checks reject bad input before anything would be launched."""
+import json
+import os
+import re
+
+import numpy as np
+import pytest
+
+from oracle import accounting, radix as oradix
+from prefix_shared_kv_gb300 import rx
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+GOLDEN = os.path.join(ROOT, "tests", "golden")
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "rx.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(rx_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_symbol(librx):
+    names = declared_functions()
+    assert len(names) >= 20
+    for n in names:
+        assert hasattr(librx, n), n
+    assert sorted(rx.EXPORTED) == names
+
+
+def test_radix_matches_oracle_on_random_sequences(librx):
+    rng = np.random.default_rng(0)
+    for trial in range(60):
+        tree, store = rx.Radix(), oradix.PrefixStore()
+        next_slot = 0
+        for _ in range(rng.integers(1, 12)):
+            base = list(rng.integers(0, 4, rng.integers(0, 30)))
+            slots = list(range(next_slot, next_slot + len(base)))
+            next_slot += len(base)
+            before = store.longest(base)
+            added = tree.insert(base, slots)
+            store.insert(base, slots)
+            assert added == len(base) - before
+        for _ in range(20):
+            q = list(rng.integers(0, 4, rng.integers(0, 35)))
+            for u in (1, 3, 16):
+                saved, slots = tree.match(q, u)
+                o_saved, o_slots = store.match(q, u)
+                assert saved == o_saved
+                assert list(slots) == list(o_slots)
+        assert tree.stats()[0] == len(store)
+
+
+def test_radix_worked_example(librx):
+    g = json.load(open(os.path.join(GOLDEN, "prefix_cache_worked_example.json")))
+    rng = np.random.default_rng(1)
+    common = rng.integers(0, 16000, g["common_prefix_tokens"])
+    tree = rx.Radix()
+    first = np.concatenate([common, rng.integers(16000, 32000, g["question_tokens"])])
+    tree.insert(first, np.arange(first.size))
+    second = np.concatenate([common, rng.integers(16000, 32000, g["question_tokens"])])
+    assert tree.match(second, 16)[0] == 992
+    assert tree.match(second, 1)[0] == 1000
+    ts = rng.integers(16000, 32000, 3)
+    assert tree.match(np.concatenate([ts, second]), 1)[0] == 0
+    assert tree.match(np.concatenate([ts, second]), 16)[0] == 0
+    np.testing.assert_array_equal(tree.match(second, 1)[1], np.arange(1000))
+
+
+def test_radix_split_keeps_first_slots_and_counts_nodes(librx):
+    t = rx.Radix()
+    assert t.insert([1, 2, 3, 4], [10, 11, 12, 13]) == 4
+    assert t.insert([1, 2, 9], [20, 21, 22]) == 1
+    assert t.stats() == (5, 3)          # root -> [1,2] -> {[3,4], [9]}
+    assert list(t.match([1, 2, 9, 7])[1]) == [10, 11, 22]
+    assert t.insert([1, 2], [30, 31]) == 0
+    assert t.insert([5], [40]) == 1
+    assert t.stats() == (6, 4)
+
+
+def test_accounting_matches_oracle_and_pages(librx):
+    g = json.load(open(os.path.join(GOLDEN, "closed_forms.json")))
+    for c in g["token_saving_ratio"]["cases"]:
+        logical = c["sharing"] * (c["prefix"] + c["distinct_inferred"])
+        processed = c["prefix"] + c["sharing"] * c["distinct_inferred"]
+        v = rx.token_saving(processed, logical)
+        assert v == accounting.token_saving_ratio(processed, logical)
+        assert round(v, 1) == c["printed_percent"]
+    cr = g["compute_reduction"]
+    assert rx.compute_reduction(cr["l_prefix"], cr["l_new"]) == accounting.compute_reduction(
+        cr["l_prefix"], cr["l_new"])
+    for m in range(0, 2000, 7):
+        for u in (1, 16, 32):
+            assert rx.saved_tokens(m, u) == oradix.PrefixStore().match([], 1)[0] + m // u * u
+    assert np.isnan(rx.token_saving(1, 0))
+
+
+def _desc(rows=4, stride=64, hq=8, hkv=2, pool=128):
+    return rx.KVDesc(hq, hkv, 128, 128 ** -0.5, pool, 0x1000, rows, stride)
+
+
+def test_plan_argument_checks(librx):
+    p = rx.Plan()
+    d = _desc()
+    with pytest.raises(rx.RxError) as e:
+        rx.decode_plan(p, d, [0, 9], [5, 5])            # row 9 outside a 4-row table
+    assert e.value.status == rx.RX_ERR_RANGE
+    with pytest.raises(rx.RxError) as e:
+        rx.decode_plan(p, d, [0], [65])                 # longer than the stride
+    assert e.value.status == rx.RX_ERR_RANGE
+    with pytest.raises(rx.RxError) as e:
+        rx.decode_plan(p, d, [0, 1], [5, 3], [0, 0], [4])  # group prefix > seq_len of a member
+    assert e.value.status == rx.RX_ERR_RANGE
+    with pytest.raises(rx.RxError) as e:
+        rx.extend_plan(p, d, [0], [10], [-1])
+    assert e.value.status == rx.RX_ERR_INVALID
+    with pytest.raises(rx.RxError) as e:
+        rx.extend_plan(p, _desc(hq=6, hkv=2), [0], [1], [1])
+    assert e.value.status == rx.RX_ERR_UNSUPPORTED
+    bad = _desc()
+    bad.head_dim = 64
+    with pytest.raises(rx.RxError) as e:
+        rx.decode_plan(p, bad, [0], [1])
+    assert e.value.status == rx.RX_ERR_UNSUPPORTED
+    # a plan that was never built cannot size a workspace
+    with pytest.raises(rx.RxError):
+        rx.Plan().workspace_size()
+
+
+def test_plans_size_workspaces_without_a_gpu(librx):
+    p = rx.Plan()
+    d = _desc(rows=8, stride=4096, hq=32, hkv=8)
+    rx.decode_plan(p, d, list(range(8)), [3000] * 8, [0] * 4 + [1] * 4, [2000, 1000])
+    n_dec = p.workspace_size()
+    # partials: every unit keeps one fp32 row of 128 + lse per (KV head, query row)
+    assert n_dec > 8 * 32 * 129 * 4
+    rx.extend_plan(p, d, list(range(8)), [2000] * 8, [100] * 8, [0] * 8, [2000])
+    assert 256 < p.workspace_size() < n_dec
+    # using an extend plan for decode is rejected before any launch
+    with pytest.raises(rx.RxError) as e:
+        rx.decode_attn(p, d, 16, 16, 16, 16, 16, None, stream=0)
+    assert e.value.status == rx.RX_ERR_INVALID

@@ -1,0 +1,199 @@
+"""Parity of the CUDA path (called through the C ABI) with the fp64 oracle.
+
+Tolerances (bf16 in, fp32 accumulate, bf16 out): O max-abs <= 2e-2 and mean-abs <= 2e-3, LSE
+within 1e-3; the pool scatter is bit-exact.  Small cases are compared element by element over every
+row; the full-size workloads, run in the benchmark's launch configuration, are compared on a
+sample of requests that the oracle computes one by one.
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle import attention as A
+from prefix_shared_kv_gb300 import rx, workloads as W
+from prefix_shared_kv_gb300.session import DeviceWorkload, bits_of, to_bf16, to_i32
+
+pytestmark = pytest.mark.gpu
+
+MAX_ABS, MEAN_ABS, LSE_ABS = 2e-2, 2e-3, 1e-3
+
+
+def assert_close(o_gpu, lse_gpu, o_ref, lse_ref, rows=None, what=""):
+    o = A.bf16_to_f64(bits_of(o_gpu))
+    l = lse_gpu.double().cpu().numpy()
+    if rows is not None:
+        o, l, o_ref, lse_ref = o[rows], l[rows], o_ref[rows], lse_ref[rows]
+    assert np.isfinite(o_ref).all()
+    err = np.abs(o - o_ref)
+    lerr = np.abs(l - lse_ref)
+    assert err.max() <= MAX_ABS, f"{what}: O max-abs {err.max():.3e}"
+    assert err.mean() <= MEAN_ABS, f"{what}: O mean-abs {err.mean():.3e}"
+    assert lerr.max() <= LSE_ABS, f"{what}: LSE max-abs {lerr.max():.3e}"
+
+
+def oracle_pools(wl, upto_step):
+    kp, vp = wl.k_pool, wl.v_pool
+    for s in range(upto_step + 1):
+        st = wl.steps[s]
+        kp, vp = A.store_kv(kp, vp, st.k_new, st.v_new, st.store_slots)
+    return kp, vp
+
+
+def run_and_check(wl, cuda, sample=None, seed=0):
+    dw = DeviceWorkload(wl, cuda)
+    rng = np.random.default_rng(seed)
+    for i, st in enumerate(wl.steps):
+        dw.run_step(i)
+        torch.cuda.synchronize()
+        kp, vp = oracle_pools(wl, i)
+        if st.extend is not None:
+            e = st.extend
+            reqs = None
+            rows = None
+            if sample is not None and len(e.req_idx) > sample:
+                reqs = sorted(rng.choice(len(e.req_idx), sample, replace=False))
+                rows = np.concatenate([np.arange(e.cu_q[r], e.cu_q[r + 1]) for r in reqs])
+            o, l = A.extend(e.q, kp, vp, wl.req_to_token, e.req_idx, e.prefix_len, e.extend_len,
+                            e.cu_q, wl.softmax_scale, requests=reqs)
+            if rows is None:
+                rows = np.arange(e.q.shape[0])
+            assert_close(dw.steps[i].ext_o, dw.steps[i].ext_lse, o, l, rows, f"{wl.name} extend")
+        if st.decode is not None:
+            d = st.decode
+            reqs = None
+            if sample is not None and len(d.req_idx) > sample:
+                reqs = sorted(rng.choice(len(d.req_idx), sample, replace=False))
+            o, l = A.decode(d.q, kp, vp, wl.req_to_token, d.req_idx, d.seq_len, wl.softmax_scale,
+                            requests=reqs)
+            rows = np.arange(len(d.req_idx)) if reqs is None else np.asarray(reqs)
+            assert_close(dw.steps[i].dec_o, dw.steps[i].dec_lse, o, l, rows, f"{wl.name} decode")
+    return dw
+
+
+# ---------------------------------------------------------------------------------------------
+# rx_store_kv
+# ---------------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("hkv,T", [(2, 1), (8, 37), (32, 1000), (1, 0)])
+def test_store_kv_bit_exact(cuda, hkv, T):
+    rng = np.random.default_rng(T)
+    P = 3000
+    sentinel = np.uint16(0x7FC1)
+    kp = np.full((P, hkv, 128), sentinel, np.uint16)
+    vp = kp.copy()
+    slots = rng.permutation(P)[:T].astype(np.int32)
+    kn, vn = W.normal_bf16(rng, (T, hkv, 128)), W.normal_bf16(rng, (T, hkv, 128))
+    dk, dv = to_bf16(kp, cuda), to_bf16(vp, cuda)
+    r2t = to_i32(np.zeros((1, 16), np.int32), cuda)
+    desc = rx.kv_desc(hkv, hkv, P, r2t)
+    rx.store_kv(desc, dk, dv, to_bf16(kn, cuda), to_bf16(vn, cuda), to_i32(slots, cuda))
+    torch.cuda.synchronize()
+    ek, ev = A.store_kv(kp, vp, kn, vn, slots)
+    np.testing.assert_array_equal(bits_of(dk), ek)
+    np.testing.assert_array_equal(bits_of(dv), ev)
+
+
+def test_store_kv_skips_out_of_range_slots(cuda):
+    rng = np.random.default_rng(5)
+    P, T = 100, 6
+    kp = np.zeros((P, 2, 128), np.uint16)
+    slots = np.array([3, -1, 50, 100, 99, 2 ** 30], np.int32)
+    kn, vn = W.normal_bf16(rng, (T, 2, 128)), W.normal_bf16(rng, (T, 2, 128))
+    dk, dv = to_bf16(kp, cuda), to_bf16(kp, cuda)
+    desc = rx.kv_desc(2, 2, P, to_i32(np.zeros((1, 16), np.int32), cuda))
+    rx.store_kv(desc, dk, dv, to_bf16(kn, cuda), to_bf16(vn, cuda), to_i32(slots, cuda))
+    torch.cuda.synchronize()
+    ok = [0, 2, 4]
+    ek, _ = A.store_kv(kp, kp, kn[ok], vn[ok], slots[ok])
+    np.testing.assert_array_equal(bits_of(dk), ek)
+
+
+# ---------------------------------------------------------------------------------------------
+# The tiny workload: 4 x 40 extend on a shared 1000-token prefix, then 8 decode steps.
+# ---------------------------------------------------------------------------------------------
+
+def test_tiny_workload_all_steps(cuda):
+    run_and_check(W.tiny(), cuda)
+
+
+# ---------------------------------------------------------------------------------------------
+# Extend: head ratios, ragged tails, own cached parts, ungrouped requests, several tiles.
+# ---------------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("hq,hkv", [(4, 4), (8, 2), (16, 2), (8, 4)])
+def test_extend_shapes(cuda, hq, hkv):
+    wl = W.extend_workload(100 + hq + hkv, hq, hkv, n_groups=2, members=5, prefix=333,
+                           ext_lo=1, ext_hi=150, own_cached_hi=70, ungrouped=2,
+                           ungrouped_prefix=129)
+    run_and_check(wl, cuda)
+
+
+def test_extend_long_causal_and_empty(cuda):
+    # prefix 0 full prefill longer than several tiles, and requests with nothing to extend
+    wl = W.extend_workload(7, 8, 8, n_groups=1, members=3, prefix=65, ext_lo=0, ext_hi=3,
+                           ungrouped=2, ungrouped_prefix=0)
+    run_and_check(wl, cuda)
+    wl = W.extend_workload(8, 8, 8, n_groups=0, members=0, prefix=0, ext_lo=300, ext_hi=700,
+                           ungrouped=2, ungrouped_prefix=0)
+    run_and_check(wl, cuda)
+
+
+def test_extend_peaky_softmax(cuda):
+    wl = W.extend_workload(9, 8, 2, n_groups=1, members=4, prefix=200, ext_lo=30, ext_hi=90)
+    for st in wl.steps:
+        q = A.bf16_to_f64(st.extend.q) * 4.0
+        st.extend.q = W.bf16_bits(q.astype(np.float32))
+    run_and_check(wl, cuda)
+
+
+# ---------------------------------------------------------------------------------------------
+# Decode: groups of many members, single-member groups, empty own parts, long prefixes.
+# ---------------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("hq,hkv", [(8, 8), (8, 2), (32, 4), (16, 8)])
+def test_decode_shapes(cuda, hq, hkv):
+    wl = W.decode_workload(200 + hq + hkv, hq, hkv, n_groups=3, members=21, prefix=777,
+                           dist_lo=1, dist_hi=300, ungrouped=3)
+    run_and_check(wl, cuda)
+
+
+def test_decode_long_prefix_many_chunks(cuda):
+    wl = W.decode_workload(11, 8, 8, n_groups=2, members=2, prefix=9000, dist_lo=1, dist_hi=3000)
+    run_and_check(wl, cuda)
+    wl = W.decode_workload(12, 32, 8, n_groups=1, members=1, prefix=5000, dist_lo=1, dist_hi=1)
+    run_and_check(wl, cuda)
+
+
+def test_decode_group_prefix_zero_and_ungrouped_only(cuda):
+    wl = W.decode_workload(13, 8, 4, n_groups=2, members=3, prefix=0, dist_lo=1, dist_hi=90,
+                           ungrouped=5)
+    run_and_check(wl, cuda)
+
+
+def test_decode_grouping_does_not_change_the_result(cuda):
+    wl = W.decode_workload(14, 16, 4, n_groups=2, members=9, prefix=400, dist_lo=20, dist_hi=200)
+    dw = DeviceWorkload(wl, cuda)
+    dw.run_step(0)
+    d = wl.steps[0].decode
+    plan = rx.Plan()
+    rx.decode_plan(plan, dw.desc, d.req_idx, d.seq_len)          # no groups declared
+    ws = torch.empty(plan.workspace_size(), dtype=torch.uint8, device=cuda)
+    plan.upload(ws)
+    o2 = torch.empty_like(dw.steps[0].dec_o)
+    l2 = torch.empty_like(dw.steps[0].dec_lse)
+    rx.decode_attn(plan, dw.desc, dw.k_pool, dw.v_pool, dw.steps[0].dec_q, o2, l2, ws)
+    torch.cuda.synchronize()
+    a = A.bf16_to_f64(bits_of(o2))
+    b = A.bf16_to_f64(bits_of(dw.steps[0].dec_o))
+    assert np.abs(a - b).max() <= MAX_ABS
+    assert (l2 - dw.steps[0].dec_lse).abs().max().item() <= LSE_ABS
+
+
+# ---------------------------------------------------------------------------------------------
+# Full-size workloads in the benchmark's configuration, sampled requests.
+# ---------------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("name", ["extend", "decode", "gqa-decode", "radix-mixed"])
+def test_full_size_workloads_sampled(cuda, name):
+    wl = W.NAMED[name]()
+    run_and_check(wl, cuda, sample=6, seed=1)
