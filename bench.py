@@ -1,0 +1,514 @@
+#!/usr/bin/env python3
+"""Benchmark of the prefix-shared KV attention path on one GB300 per rank.
+
+One step = one pass of the whole hot path over one batch: host prefix match of the batch's
+requests (radix cache), rx_store_kv of the step's new tokens, rx_extend_attn and rx_decode_attn.
+The default workload is the radix-tree mixed batch (1000-token system prompt -> 8 x 500 -> 32 x
+200 leaves; 16 leaf requests extend 64 tokens, 8 cache misses prefill 1500 tokens, 40 decode
+requests), the one batch that exercises every part of the path.
+
+Printed metric (one JSON line on rank 0): `value` = extend FLOPs of the batch divided by the device
+time of the whole step (store + extend + decode), in TFLOP/s; `parts` gives each part against its
+own roofline (decode: unique KV bytes / time vs HBM; extend: FLOPs / time vs bf16 tensor peak;
+store: bytes moved / time).  Decode-only workloads report decode GB/s instead.
+
+Timing: W warm-up steps, then K steps, each bracketed by CUDA events on the launch stream with a
+256 MiB L2 flush between steps (outside the events); barrier + synchronize on both sides; max over
+ranks.  `--impl reference` times the fp64 oracle on host cores on a bounded sample instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "prefix-shared attn: decode KV GB/s (% HBM peak); extend TFLOP/s (% BF16 peak)"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ---------------------------------------------------------------------------------------------
+# Algorithmic work of a workload (what the method must compute / move, nothing more)
+# ---------------------------------------------------------------------------------------------
+
+def work_counts(wl, step=0):
+    st = wl.steps[step]
+    d, hq, hkv = wl.head_dim, wl.num_q_heads, wl.num_kv_heads
+    out = {"extend_flops": 0.0, "decode_kv_bytes": 0.0, "store_bytes": 0.0,
+           "extend_rows": 0, "decode_rows": 0}
+    out["store_bytes"] = float(len(st.store_slots)) * hkv * d * 2 * 2 * 2  # K,V x read+write
+    if st.extend is not None:
+        e = st.extend
+        p = e.prefix_len.astype(np.float64)
+        E = e.extend_len.astype(np.float64)
+        out["extend_flops"] = float(4.0 * d * hq * np.sum(E * p + E * (E + 1) / 2))
+        out["extend_rows"] = int(E.sum())
+    if st.decode is not None:
+        dc = st.decode
+        gp = np.where(dc.group_of_req >= 0,
+                      dc.group_prefix_len[np.maximum(dc.group_of_req, 0)] if len(dc.group_prefix_len) else 0,
+                      0)
+        used = set(int(g) for g in dc.group_of_req if g >= 0)
+        tokens = float(np.sum(dc.seq_len - gp)) + float(sum(dc.group_prefix_len[g] for g in used))
+        out["decode_kv_bytes"] = tokens * hkv * d * 2 * 2
+        out["decode_rows"] = int(len(dc.req_idx))
+    return out
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return {k: float(pk[k]) for k in FALLBACK_PEAKS}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ---------------------------------------------------------------------------------------------
+# Clocks during the timed region
+# ---------------------------------------------------------------------------------------------
+
+class ClockSampler:
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        try:
+            for line in open(self.path):
+                f = [x.strip() for x in line.split(",")]
+                if len(f) < 9:
+                    continue
+                try:
+                    sm.append(float(f[1]))
+                    mx.append(float(f[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, f[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        finally:
+            os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------------------------------
+# Oracle (CPU) timing on a bounded sample -- the reference arm and the cpu_baseline
+# ---------------------------------------------------------------------------------------------
+
+def oracle_sample_rate(wl, budget_s=12.0):
+    """Time the fp64 oracle on a bounded sample of the step and scale it to the whole step.
+    Returns (extend TFLOP/s equivalent, decode GB/s equivalent, est. step seconds, sample text,
+    threads)."""
+    from oracle import attention as A
+    st = wl.steps[0]
+    kp, vp = A.store_kv(wl.k_pool, wl.v_pool, st.k_new, st.v_new, st.store_slots)
+    w = work_counts(wl)
+    d, hq = wl.head_dim, wl.num_q_heads
+    t_ext = t_dec = 0.0
+    f_done = b_done = 0.0
+    n_ext = n_dec = 0
+    if st.extend is not None:
+        e = st.extend
+        order = np.argsort(-(e.extend_len.astype(np.int64)))  # mix long and short requests
+        order = np.concatenate([order[::2], order[1::2]])
+        t0 = time.perf_counter()
+        for r in order:
+            if e.extend_len[r] == 0:
+                continue
+            A.extend(e.q, kp, vp, wl.req_to_token, e.req_idx, e.prefix_len, e.extend_len, e.cu_q,
+                     wl.softmax_scale, requests=[int(r)])
+            E, p = float(e.extend_len[r]), float(e.prefix_len[r])
+            f_done += 4.0 * d * hq * (E * p + E * (E + 1) / 2)
+            n_ext += 1
+            if time.perf_counter() - t0 > budget_s * (0.7 if st.decode is not None else 1.0):
+                break
+        t_ext = time.perf_counter() - t0
+    if st.decode is not None:
+        dc = st.decode
+        t0 = time.perf_counter()
+        gp_of = lambda b: dc.group_prefix_len[dc.group_of_req[b]] if dc.group_of_req[b] >= 0 else 0
+        for b in range(len(dc.req_idx)):
+            A.decode(dc.q, kp, vp, wl.req_to_token, dc.req_idx, dc.seq_len, wl.softmax_scale,
+                     requests=[b])
+            # the oracle reads every key of the request; count the bytes the method must move
+            b_done += float(dc.seq_len[b]) * wl.num_kv_heads * d * 4
+            n_dec += 1
+            if time.perf_counter() - t0 > budget_s * (0.3 if st.extend is not None else 1.0):
+                break
+        t_dec = time.perf_counter() - t0
+    est = 0.0
+    if f_done > 0:
+        est += t_ext * w["extend_flops"] / f_done
+    if b_done > 0:
+        naive_bytes = float(np.sum(st.decode.seq_len)) * wl.num_kv_heads * d * 4
+        est += t_dec * naive_bytes / b_done
+    ext_rate = w["extend_flops"] / est / 1e12 if est > 0 else 0.0
+    dec_rate = w["decode_kv_bytes"] / est / 1e9 if est > 0 else 0.0
+    try:
+        import threadpoolctl
+        threads = max(i.get("num_threads", 1) for i in threadpoolctl.threadpool_info()) or 1
+    except Exception:
+        threads = os.cpu_count() or 1
+    sample = (f"{n_ext} extend + {n_dec} decode requests of the batch in fp64 numpy "
+              f"({t_ext + t_dec:.1f} s), scaled to the whole step by FLOPs / KV bytes")
+    return ext_rate, dec_rate, est, sample, threads
+
+
+# ---------------------------------------------------------------------------------------------
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["rx", "reference"], default="rx")
+    ap.add_argument("--workload", default="radix-mixed",
+                    choices=["radix-mixed", "extend", "decode", "gqa-decode", "tiny"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", choices=["store", "extend", "decode"], default=None,
+                    help="time one part alone (profiling runs)")
+    return ap.parse_args()
+
+
+def dist_init():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    pg = None
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+        pg = dist
+    return rank, world, local, pg
+
+
+def barrier(pg, dev=None):
+    if pg is not None:
+        if dev is not None:
+            pg.barrier(device_ids=[dev.index])
+        else:
+            pg.barrier()
+
+
+def allreduce_max(pg, x, dev):
+    if pg is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def kernel_source_hash(name):
+    p = os.path.join(ROOT, "prefix_shared_kv_gb300", "csrc", name)
+    try:
+        return hashlib.sha1(open(p, "rb").read()).hexdigest()[:12]
+    except OSError:
+        return None
+
+
+def recorded_traffic(kernel_file, workload):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on this exact
+    kernel source (hash) and workload; else None."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    h = kernel_source_hash(kernel_file)
+    try:
+        for line in open(path):
+            f = line.split()
+            if len(f) >= 4 and f[0] == kernel_file and f[1] == workload and f[3] == h:
+                return float(f[2])
+    except OSError:
+        pass
+    return None
+
+
+def main():
+    args = parse_args()
+    from prefix_shared_kv_gb300 import workloads as W
+
+    if args.impl == "reference":
+        # the oracle on host cores; under torchrun only rank 0 runs it
+        if int(os.environ.get("RANK", "0")) != 0:
+            return 0
+        wl = W.NAMED[args.workload]()
+        w = work_counts(wl)
+        rates = []
+        t0 = time.perf_counter()
+        per = max(2.0, min(12.0, 150.0 / max(1, args.steps)))
+        for _ in range(args.steps):
+            er, dr, est, sample, threads = oracle_sample_rate(wl, budget_s=per)
+            rates.append((er, dr, est))
+        er = statistics.mean(r[0] for r in rates)
+        dr = statistics.mean(r[1] for r in rates)
+        est = statistics.mean(r[2] for r in rates)
+        primary = er if w["extend_flops"] > 0 else dr
+        unit = "TFLOP/s" if w["extend_flops"] > 0 else "GB/s"
+        line = {"impl": "reference", "metric": METRIC, "value": primary, "unit": unit,
+                "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": est * 1e3, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": {"workload": wl.name, "recipe": wl.recipe},
+                "cpu_baseline": {"value": primary, "unit": unit, "cores": threads,
+                                 "kind": "oracle", "sample": sample},
+                "e2e": {"value": primary, "unit": unit, "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0},
+                "wall_s": time.perf_counter() - t0}
+        print(json.dumps(line), flush=True)
+        return 0
+
+    rank, world, local, pg = dist_init()
+    import torch
+    from prefix_shared_kv_gb300 import rx
+    from prefix_shared_kv_gb300.session import DeviceWorkload
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    rx.lib()
+    wl = W.NAMED[args.workload]()
+    w = work_counts(wl)
+    peaks, peak_src = load_peaks()
+    dw = DeviceWorkload(wl, dev)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    parts = [("store", dw.store), ("extend", dw.extend), ("decode", dw.decode)]
+    if args.only:
+        parts = [p for p in parts if p[0] == args.only]
+
+    def step():
+        for _, f in parts:
+            f(0)
+
+    for _ in range(max(args.warmup, 0)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(dev)
+    barrier(pg, dev)
+    torch.cuda.synchronize(dev)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(parts) + 1)]
+          for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    t_wall = time.perf_counter()
+    for k in range(args.steps):
+        flush.zero_()
+        ev[k][0].record(stream)
+        for j, (_, f) in enumerate(parts):
+            f(0)
+            ev[k][j + 1].record(stream)
+    torch.cuda.synchronize(dev)
+    t_wall = time.perf_counter() - t_wall
+    barrier(pg, dev)
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    step_ms = [ev[k][0].elapsed_time(ev[k][-1]) for k in range(args.steps)]
+    part_ms = {name: statistics.mean(ev[k][j].elapsed_time(ev[k][j + 1]) for k in range(args.steps))
+               for j, (name, _) in enumerate(parts)}
+    ms = statistics.mean(step_ms)
+    ms_max = allreduce_max(pg, ms, dev)
+
+    has_ext = w["extend_flops"] > 0 and "extend" in part_ms
+    has_dec = w["decode_kv_bytes"] > 0 and "decode" in part_ms
+    units_per_step = w["extend_flops"] if has_ext else (w["decode_kv_bytes"] if has_dec else w["store_bytes"])
+    scale = 1e12 if has_ext else 1e9
+    unit = "TFLOP/s" if has_ext else "GB/s"
+    value = world * units_per_step / (ms_max * 1e-3) / scale
+
+    pdesc = {}
+    if "store" in part_ms:
+        a = w["store_bytes"] / (part_ms["store"] * 1e-3) / 1e9
+        pdesc["store"] = {"ms": part_ms["store"], "GB/s": a, "frac_hbm": a / peaks["hbm_gbs"],
+                          "bytes": w["store_bytes"]}
+    if has_ext:
+        a = w["extend_flops"] / (part_ms["extend"] * 1e-3) / 1e12
+        pdesc["extend"] = {"ms": part_ms["extend"], "TFLOP/s": a,
+                           "frac_bf16": a / peaks["bf16_tflops"], "flops": w["extend_flops"]}
+    if has_dec:
+        a = w["decode_kv_bytes"] / (part_ms["decode"] * 1e-3) / 1e9
+        pdesc["decode"] = {"ms": part_ms["decode"], "GB/s": a, "frac_hbm": a / peaks["hbm_gbs"],
+                           "unique_kv_bytes": w["decode_kv_bytes"]}
+    if has_ext:
+        dom = ("extend", "extend_attn.cu")
+        roof = {"bound": "tensor", "achieved": pdesc["extend"]["TFLOP/s"],
+                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": pdesc["extend"]["frac_bf16"]}
+    elif has_dec:
+        dom = ("decode", "decode_attn.cu")
+        roof = {"bound": "hbm", "achieved": pdesc["decode"]["GB/s"], "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": pdesc["decode"]["frac_hbm"]}
+    else:
+        dom = ("store", "store_kv.cu")
+        roof = {"bound": "hbm", "achieved": pdesc["store"]["GB/s"], "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": pdesc["store"]["frac_hbm"]}
+    roof["kernel"] = dom[0]
+    roof["peak_source"] = f"{peak_src} (burst)" if roof["unit"] == "TFLOP/s" else peak_src
+    roof["traffic"] = recorded_traffic(dom[1], wl.name)
+
+    launches_per_step = {"store": 1, "extend": 1, "decode": 2}
+    gpu_launches = args.steps * sum(launches_per_step[n] for n, _ in parts)
+
+    # ---- end to end through the public API with host buffers -----------------------------
+    e2e = None
+    if not args.no_e2e and not args.only:
+        e2e = run_e2e(wl, dw, dev, args, pg, world, w, unit, scale, has_ext)
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline and not args.only:
+        er, dr, est, sample, threads = oracle_sample_rate(wl, budget_s=12.0)
+        cpu = {"value": er if has_ext else dr, "unit": unit, "cores": threads, "kind": "oracle",
+               "sample": sample}
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": unit, "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "bf16", "data": "synthetic",
+                "config": {"workload": wl.name, "recipe": wl.recipe,
+                           "parallelism": f"replicas x{world}",
+                           "l2": "256 MiB buffer written between timed steps"},
+                "parts": pdesc, "roofline": roof, "gpu_launches": gpu_launches,
+                "clocks": clk, "e2e": e2e, "cpu_baseline": cpu, "wall_timed_s": t_wall}
+        if args.only:
+            line["only"] = args.only
+        print(json.dumps(line), flush=True)
+    if pg is not None:
+        pg.destroy_process_group()
+    return 0
+
+
+def run_e2e(wl, dw, dev, args, pg, world, w, unit, scale, has_ext):
+    """Same step through the public API with host buffers: host radix match of the extend
+    requests, plan build + upload, H2D of the step's inputs from pinned memory, the three calls,
+    D2H of O and LSE; wall clock per step after a synchronize."""
+    import torch
+    from prefix_shared_kv_gb300 import rx
+    from prefix_shared_kv_gb300.session import workspace
+
+    st = wl.steps[0]
+    ds = dw.steps[0]
+    pin = lambda t: t.cpu().pin_memory()
+    h_in = {"slots": pin(ds.slots), "k_new": pin(ds.k_new), "v_new": pin(ds.v_new)}
+    if ds.ext_q is not None:
+        h_in["ext_q"] = pin(ds.ext_q)
+    if ds.dec_q is not None:
+        h_in["dec_q"] = pin(ds.dec_q)
+    d_in = {k: torch.empty_like(v, device=dev) for k, v in h_in.items()}
+    h_out = {}
+    if ds.ext_o is not None:
+        h_out["ext_o"] = torch.empty_like(ds.ext_o, device="cpu").pin_memory()
+        h_out["ext_lse"] = torch.empty_like(ds.ext_lse, device="cpu").pin_memory()
+    if ds.dec_o is not None:
+        h_out["dec_o"] = torch.empty_like(ds.dec_o, device="cpu").pin_memory()
+        h_out["dec_lse"] = torch.empty_like(ds.dec_lse, device="cpu").pin_memory()
+    tree = rx.Radix()
+    for toks, slots in wl.cached_sequences:
+        tree.insert(toks, slots)
+    eplan, dplan = rx.Plan(), rx.Plan()
+    ews = dws = None
+    if st.extend is not None:
+        rx.extend_plan(eplan, dw.desc, st.extend.req_idx, st.extend.prefix_len,
+                       st.extend.extend_len, st.extend.group_of_req, st.extend.group_prefix_len)
+        ews = workspace(eplan.workspace_size(), dev)
+    if st.decode is not None:
+        rx.decode_plan(dplan, dw.desc, st.decode.req_idx, st.decode.seq_len,
+                       st.decode.group_of_req, st.decode.group_prefix_len)
+        dws = workspace(dplan.workspace_size(), dev)
+    h2d = sum(v.numel() * v.element_size() for v in h_in.values())
+    d2h = sum(v.numel() * v.element_size() for v in h_out.values())
+    if st.extend is not None:
+        # the cache hit of every extend request must be the prefix the workload cached
+        for r, toks in enumerate(st.extend.tokens):
+            assert tree.match(toks, 1, want_slots=False) == int(st.extend.prefix_len[r])
+
+    def one():
+        # a2: prefix match of the extend requests against the radix cache (host)
+        if st.extend is not None:
+            e = st.extend
+            pl = np.fromiter((tree.match(t, 1, want_slots=False) for t in e.tokens), np.int32,
+                             count=len(e.tokens))
+            rx.extend_plan(eplan, dw.desc, e.req_idx, pl, e.extend_len, e.group_of_req,
+                           e.group_prefix_len)
+            eplan.upload(ews)
+        if st.decode is not None:
+            dc = st.decode
+            rx.decode_plan(dplan, dw.desc, dc.req_idx, dc.seq_len, dc.group_of_req,
+                           dc.group_prefix_len)
+            dplan.upload(dws)
+        for k in h_in:
+            d_in[k].copy_(h_in[k], non_blocking=True)
+        rx.store_kv(dw.desc, dw.k_pool, dw.v_pool, d_in["k_new"], d_in["v_new"], d_in["slots"])
+        if st.extend is not None:
+            rx.extend_attn(eplan, dw.desc, dw.k_pool, dw.v_pool, d_in["ext_q"], ds.ext_o,
+                           ds.ext_lse, ews)
+            h_out["ext_o"].copy_(ds.ext_o, non_blocking=True)
+            h_out["ext_lse"].copy_(ds.ext_lse, non_blocking=True)
+        if st.decode is not None:
+            rx.decode_attn(dplan, dw.desc, dw.k_pool, dw.v_pool, d_in["dec_q"], ds.dec_o,
+                           ds.dec_lse, dws)
+            h_out["dec_o"].copy_(ds.dec_o, non_blocking=True)
+            h_out["dec_lse"].copy_(ds.dec_lse, non_blocking=True)
+        torch.cuda.synchronize(dev)
+
+    for _ in range(max(3, args.warmup)):
+        one()
+    barrier(pg, dev)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        one()
+        times.append(time.perf_counter() - t0)
+    barrier(pg, dev)
+    ms = allreduce_max(pg, statistics.mean(times) * 1e3, dev)
+    units = w["extend_flops"] if has_ext else w["decode_kv_bytes"]
+    return {"value": world * units / (ms * 1e-3) / scale, "unit": unit, "ms_per_step": ms,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "note": "per step: host radix match, plan build + upload, H2D, kernels, D2H"}
+
+
+if __name__ == "__main__":
+    sys.exit(main())
