@@ -9,13 +9,25 @@
 // keys (visible to that member's rows only, causal on its new tokens).  One online softmax runs
 // across all segments, so no partial results leave the CTA.
 //
-// This file holds the mma.m16n8k16 version of the tile loop: 8 warps x 16 rows, 64 keys per
-// stage, 3-stage cp.async ring of swizzled K/V rows gathered by slot.
+// Blackwell tile loop (one CTA per work item, 256 threads, warp-specialised):
+//   warps 5-7  producers: gather the next 128 keys' K and V rows by slot with 16-byte cp.async
+//              into a 2-stage ring laid out as 128-byte-swizzled UMMA tiles; completion is
+//              signalled per stage with cp.async.mbarrier.arrive;
+//   warp 4     MMA issuer (one thread): S = Q K^T with tcgen05.mma (both operands K-major in
+//              shared memory, fp32 accumulator in TMEM, double-buffered), then O += P V with P
+//              read from TMEM and V as an MN-major shared-memory operand;
+//   warps 0-3  softmax: thread r owns query row r (TMEM lane r): tcgen05.ld of its S row, masks,
+//              online max / sum in base 2 (the running max is only moved -- and O in TMEM rescaled
+//              -- when it grows by more than 2^8), P = exp2(.) packed to bf16 and written to its own
+//              TMEM columns with tcgen05.st for the PV MMA; finally O / l and the LSE.
+// Every mbarrier wait is bounded (globaltimer); a timeout records RX_ERR_TIMEOUT in the
+// workspace status word and every role leaves its loop.
 #include <cuda_runtime.h>
 #include <math_constants.h>
 
 #include "ptx.cuh"
 #include "rx_internal.h"
+#include "tc.cuh"
 
 namespace rx {
 namespace {
@@ -38,229 +50,321 @@ struct ExtParams {
 };
 
 constexpr int kThreads = 256;
-constexpr int kNK = 64;
-constexpr int kStages = 3;
-constexpr int kHalf = kNK * kHeadDim * 2;       // 16 KiB: K (or V) rows of one stage
-constexpr int kStage = 2 * kHalf;               // 32 KiB
+constexpr int kProducers = 96;          // warps 5..7
+constexpr int kN = 128;                 // keys per tile
+constexpr int kStages = 2;
 constexpr int kMaxSegs = 1 + 128;
-constexpr size_t kSmem = (size_t)kStages * kStage + kMaxSegs * sizeof(ExtSeg);
+constexpr int kHalfBlock = 128 * 128;   // one 64-column half of a 128-row tile: 16 KiB
+constexpr int kTile = 2 * kHalfBlock;   // 128 rows x 128 bf16: 32 KiB
+constexpr int kOffQ = 0;
+constexpr int kOffStage = kTile;                        // stage s: K at +s*2*kTile, V after it
+constexpr int kOffSlots = kOffStage + kStages * 2 * kTile;
+constexpr int kOffSegs = kOffSlots + kStages * kN * 4;
+constexpr int kOffBar = kOffSegs + kMaxSegs * 16;
+enum { B_KV_FULL = 0, B_KV_EMPTY = 2, B_Q_FULL = 4, B_S_FULL = 5, B_P_FULL = 7, B_PV_DONE = 9,
+       B_FINAL = 10, B_COUNT = 11 };
+constexpr int kOffTmem = kOffBar + B_COUNT * 8;
+constexpr int kOffAbort = kOffTmem + 8;
+constexpr size_t kSmem = 1024 + kOffAbort + 16;
+constexpr uint32_t kTmemCols = 512;     // S0 [0,128), S1 [128,256), O [256,384), P0, P1 64 each
+constexpr uint32_t kColO = 256;
+constexpr uint32_t kColP = 384;
+constexpr uint64_t kWaitNs = 2000000000ull;
 
-struct Cursor {
+static_assert(kSmem <= 227 * 1024, "shared memory budget");
+
+struct TileIter {
   int seg, k0;
 };
-
-__device__ __forceinline__ void advance(Cursor& c, const ExtSeg* segs, int n_seg) {
-  c.k0 += kNK;
+__device__ __forceinline__ void tile_next(TileIter& c, const ExtSeg* segs, int n_seg) {
+  c.k0 += kN;
   if (c.k0 >= segs[c.seg].k_end) {
     ++c.seg;
     if (c.seg < n_seg) c.k0 = segs[c.seg].k_begin;
   }
 }
 
-__device__ __forceinline__ void load_tile(const ExtParams& p, const ExtSeg& sg, int k0, int kv_head,
-                                          uint32_t kb) {
-  const int32_t* r2t = p.req_to_token + (int64_t)sg.kv_row * p.stride;
-#pragma unroll
-  for (int u = 0; u < kNK * 16 / kThreads; ++u) {
-    const int i = threadIdx.x + u * kThreads;
-    const int key = i / 16, c = i % 16;
-    const int kpos = k0 + key;
-    int slot = kpos < sg.k_end ? __ldg(r2t + kpos) : -1;
-    if (kpos < sg.k_end && (slot < 0 || slot >= p.pool_size)) {  // outside the pool: flag, skip
-      atomicCAS(p.status, 0, (int)RX_ERR_RANGE);
-      slot = -1;
-    }
-    const bool ok = slot >= 0;
-    const int64_t off = ok ? ((int64_t)slot * p.hkv + kv_head) * kHeadDim + c * 8 : 0;
-    const uint32_t so = swz256(key, c);
-    cp_async16(kb + so, p.k_pool + off, ok);
-    cp_async16(kb + kHalf + so, p.v_pool + off, ok);
-  }
+// byte offset of 16-byte chunk c (0..15) of row r in a K-major 128-row tile (two SW128 halves)
+__device__ __forceinline__ uint32_t tile_off(int r, int c) {
+  return (uint32_t)((c >> 3) * kHalfBlock + r * 128 + (((c & 7) ^ (r & 7)) << 4));
 }
 
-__global__ void __launch_bounds__(kThreads, 1) extend_mma_kernel(ExtParams p) {
-  extern __shared__ __align__(1024) uint8_t smem[];
-  const ExtItem it = p.items[blockIdx.x];
-  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const uint32_t sbase = smem_u32(smem);
-  ExtSeg* s_segs = reinterpret_cast<ExtSeg*>(smem + kStages * kStage);
-  for (int i = threadIdx.x; i < it.n_seg; i += kThreads) s_segs[i] = p.segs[it.seg_begin + i];
+// Named barrier over `n` threads that also ORs a predicate across them.
+__device__ __forceinline__ bool bar_any(int id, int n, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n.reg .pred p, q;\nsetp.ne.u32 p, %1, 0;\nbar.red.or.pred q, %2, %3, p;\n"
+      "selp.u32 %0, 1, 0, q;\n}\n"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "r"(id), "r"(n)
+      : "memory");
+  return r != 0;
+}
 
-  // Query rows (token t = r / gq, query head kv_head*gq + r % gq) -> stage 2.
-  const uint32_t qb = sbase + 2 * kStage;
+__device__ __forceinline__ void cp_async_mbar_arrive(uint32_t mbar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(mbar) : "memory");
+}
+
+__device__ __forceinline__ void producer(const ExtParams& p, const ExtItem& it,
+                                         const ExtSeg* segs, int ntiles, uint32_t base,
+                                         uint8_t* sp, volatile int* abort) {
+  const int ptid = threadIdx.x - 160;
   const int n_rows = it.n_tok * p.gq;
-  for (int i = threadIdx.x; i < 128 * 16; i += kThreads) {
-    const int r = i / 16, c = i % 16;
+  // query tile
+  for (int i = ptid; i < 128 * 16; i += kProducers) {
+    const int r = i >> 4, c = i & 15;
     const bool ok = r < n_rows;
     const __nv_bfloat16* src =
         ok ? p.q + ((int64_t)p.rows[it.row_begin + r / p.gq].q_row * p.hq + it.kv_head * p.gq +
                     r % p.gq) * kHeadDim + c * 8
            : p.q;
-    cp_async16(qb + swz256(r, c), src, ok);
+    cp_async16(base + kOffQ + tile_off(r, c), src, ok);
   }
-  cp_async_commit();
-  __syncthreads();  // segments visible
-
-  // Row metadata of this thread's two rows.
-  const int r0 = warp * 16 + lane / 4, r1 = r0 + 8;
-  int own0 = -2, own1 = -2, kmx0 = 0, kmx1 = 0, qrow0 = 0, qrow1 = 0;
-  if (r0 < n_rows) {
-    const ExtRow e = p.rows[it.row_begin + r0 / p.gq];
-    own0 = e.owner; kmx0 = e.kmax; qrow0 = e.q_row;
-  }
-  if (r1 < n_rows) {
-    const ExtRow e = p.rows[it.row_begin + r1 / p.gq];
-    own1 = e.owner; kmx1 = e.kmax; qrow1 = e.q_row;
-  }
-  const int w_lo = __reduce_min_sync(0xffffffffu, min(r0 < n_rows ? own0 : INT_MAX,
-                                                      r1 < n_rows ? own1 : INT_MAX));
-  const int w_hi = __reduce_max_sync(0xffffffffu, max(r0 < n_rows ? own0 : -1,
-                                                      r1 < n_rows ? own1 : -1));
-  const int w_kmax = __reduce_max_sync(0xffffffffu, max(kmx0, kmx1));
-
-  int ntiles = 0;
-  for (int s = 0; s < it.n_seg; ++s) ntiles += (s_segs[s].k_end - s_segs[s].k_begin + kNK - 1) / kNK;
-
-  Cursor ld{0, it.n_seg > 0 ? s_segs[0].k_begin : 0};
-  for (int pre = 0; pre < 2; ++pre) {
-    if (pre < ntiles) {
-      load_tile(p, s_segs[ld.seg], ld.k0, it.kv_head, sbase + pre * kStage);
-      advance(ld, s_segs, it.n_seg);
-    }
-    cp_async_commit();
-  }
-  cp_async_wait<2>();
-  __syncthreads();
-  uint32_t qf[8][4];
-  {
-    const int r = warp * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
-#pragma unroll
-    for (int kk = 0; kk < 8; ++kk)
-      ldsm_x4(qb + swz256(r, 2 * kk + (lane >> 4)), qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3]);
-  }
-  __syncthreads();
-
-  float o[16][4];
-#pragma unroll
-  for (int n = 0; n < 16; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
-  float m0 = -CUDART_INF_F, m1 = -CUDART_INF_F, l0 = 0.f, l1 = 0.f;
-  Cursor cc{0, it.n_seg > 0 ? s_segs[0].k_begin : 0};
-
+  cp_async_mbar_arrive(base + kOffBar + 8 * B_Q_FULL);
+  TileIter cur{0, segs[0].k_begin};
   for (int t = 0; t < ntiles; ++t) {
-    if (t + 2 < ntiles) {
-      load_tile(p, s_segs[ld.seg], ld.k0, it.kv_head, sbase + ((t + 2) % kStages) * kStage);
-      advance(ld, s_segs, it.n_seg);
+    const int st = t & 1;
+    const bool waited = t < kStages ||
+        tc::mbar_wait(base + kOffBar + 8 * (B_KV_EMPTY + st), ((t >> 1) - 1) & 1, abort,
+                      p.status, kWaitNs);
+    const ExtSeg sg = segs[cur.seg];
+    int32_t* slots = reinterpret_cast<int32_t*>(sp + kOffSlots) + st * kN;
+    const int32_t* r2t = p.req_to_token + (int64_t)sg.kv_row * p.stride;
+    for (int k = ptid; waited && k < kN; k += kProducers) {
+      const int kpos = cur.k0 + k;
+      int s = kpos < sg.k_end ? __ldg(r2t + kpos) : -1;
+      if (kpos < sg.k_end && (s < 0 || s >= p.pool_size)) {  // outside the pool: flag, skip
+        atomicCAS(p.status, 0, (int)RX_ERR_RANGE);
+        s = -1;
+      }
+      slots[k] = s;
     }
-    cp_async_commit();
-    cp_async_wait<2>();
-    __syncthreads();
-
-    const ExtSeg sg = s_segs[cc.seg];
-    const int k0 = cc.k0;
-    const bool active = (sg.owner < 0 || (sg.owner >= w_lo && sg.owner <= w_hi)) && k0 < w_kmax;
-    if (active) {
-      const uint32_t kb = sbase + (t % kStages) * kStage;
-      const uint32_t vb = kb + kHalf;
-      float s[8][4];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
-#pragma unroll
-        for (int k2 = 0; k2 < 4; ++k2) {
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4(kb + swz256(8 * j + (lane & 7), 4 * k2 + (lane >> 3)), b0, b1, b2, b3);
-          mma_16816(s[j], qf[2 * k2], b0, b1);
-          mma_16816(s[j], qf[2 * k2 + 1], b2, b3);
-        }
-      }
-      const bool vis0 = sg.owner < 0 || sg.owner == own0;
-      const bool vis1 = sg.owner < 0 || sg.owner == own1;
-      const int lim0 = vis0 ? min(kmx0, sg.k_end) : INT_MIN;
-      const int lim1 = vis1 ? min(kmx1, sg.k_end) : INT_MIN;
-      float mx0 = -CUDART_INF_F, mx1 = -CUDART_INF_F;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int kp = k0 + 8 * j + 2 * (lane & 3);
-        s[j][0] = (kp < lim0) ? s[j][0] * p.scale_log2 : -CUDART_INF_F;
-        s[j][1] = (kp + 1 < lim0) ? s[j][1] * p.scale_log2 : -CUDART_INF_F;
-        s[j][2] = (kp < lim1) ? s[j][2] * p.scale_log2 : -CUDART_INF_F;
-        s[j][3] = (kp + 1 < lim1) ? s[j][3] * p.scale_log2 : -CUDART_INF_F;
-        mx0 = fmaxf(mx0, fmaxf(s[j][0], s[j][1]));
-        mx1 = fmaxf(mx1, fmaxf(s[j][2], s[j][3]));
-      }
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-      const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
-      const float b0s = (n0 == -CUDART_INF_F) ? 0.f : n0;
-      const float b1s = (n1 == -CUDART_INF_F) ? 0.f : n1;
-      const float a0 = fast_exp2(m0 - b0s), a1 = fast_exp2(m1 - b1s);
-      m0 = n0;
-      m1 = n1;
-      float ps0 = 0.f, ps1 = 0.f;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        s[j][0] = fast_exp2(s[j][0] - b0s);
-        s[j][1] = fast_exp2(s[j][1] - b0s);
-        s[j][2] = fast_exp2(s[j][2] - b1s);
-        s[j][3] = fast_exp2(s[j][3] - b1s);
-        ps0 += s[j][0] + s[j][1];
-        ps1 += s[j][2] + s[j][3];
-      }
-      l0 = l0 * a0 + ps0;
-      l1 = l1 * a1 + ps1;
-#pragma unroll
-      for (int n = 0; n < 16; ++n) {
-        o[n][0] *= a0;
-        o[n][1] *= a0;
-        o[n][2] *= a1;
-        o[n][3] *= a1;
-      }
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        const uint32_t a[4] = {pack_bf16(s[2 * kk][0], s[2 * kk][1]),
-                               pack_bf16(s[2 * kk][2], s[2 * kk][3]),
-                               pack_bf16(s[2 * kk + 1][0], s[2 * kk + 1][1]),
-                               pack_bf16(s[2 * kk + 1][2], s[2 * kk + 1][3])};
-        const int vr = 16 * kk + (lane & 7) + ((lane >> 3) & 1) * 8;
-#pragma unroll
-        for (int n2 = 0; n2 < 8; ++n2) {
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4_t(vb + swz256(vr, 2 * n2 + (lane >> 4)), b0, b1, b2, b3);
-          mma_16816(o[2 * n2], a, b0, b1);
-          mma_16816(o[2 * n2 + 1], a, b2, b3);
-        }
-      }
+    // slots visible to all producers; leave together if any of them gave up waiting
+    if (bar_any(1, kProducers, !waited || *abort)) break;
+    const uint32_t kb = base + kOffStage + st * 2 * kTile;
+    for (int i = ptid; i < kN * 16; i += kProducers) {
+      const int key = i >> 4, c = i & 15;
+      const int s = slots[key];
+      const int64_t off = s >= 0 ? ((int64_t)s * p.hkv + it.kv_head) * kHeadDim + c * 8 : 0;
+      const uint32_t so = tile_off(key, c);
+      cp_async16(kb + so, p.k_pool + off, s >= 0);
+      cp_async16(kb + kTile + so, p.v_pool + off, s >= 0);
     }
-    advance(cc, s_segs, it.n_seg);
-    __syncthreads();
+    cp_async_mbar_arrive(base + kOffBar + 8 * (B_KV_FULL + st));
+    tile_next(cur, segs, it.n_seg);
   }
+  cp_async_wait<0>();
+}
 
-  l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-  l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-  l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-  l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-  const float inv0 = l0 > 0.f ? 1.f / l0 : 0.f, inv1 = l1 > 0.f ? 1.f / l1 : 0.f;
-  if (r0 < n_rows) {
-    const int qh = it.kv_head * p.gq + r0 % p.gq;
-    __nv_bfloat16* dst = p.o + ((int64_t)qrow0 * p.hq + qh) * kHeadDim + 2 * (lane & 3);
+__device__ __forceinline__ void mma_issuer(const ExtParams& p, int ntiles, uint32_t base,
+                                           uint32_t tmem, volatile int* abort) {
+  constexpr uint32_t idS = tc::idesc_bf16(128, kN, false, false);
+  constexpr uint32_t idO = tc::idesc_bf16(128, 128, false, true);
+  const uint32_t bar = base + kOffBar;
+  auto pv = [&](int u) -> bool {
+    if (!tc::mbar_wait(bar + 8 * (B_P_FULL + (u & 1)), (u >> 1) & 1, abort, p.status, kWaitNs))
+      return false;
+    tc::fence_after();
+    const uint32_t vb = base + kOffStage + (u & 1) * 2 * kTile + kTile;
+    const uint32_t pcol = tmem + kColP + (u & 1) * 64;
 #pragma unroll
-    for (int n = 0; n < 16; ++n)
-      *reinterpret_cast<uint32_t*>(dst + 8 * n) = pack_bf16(o[n][0] * inv0, o[n][1] * inv0);
-    if ((lane & 3) == 0)
-      p.lse[(int64_t)qrow0 * p.hq + qh] =
-          l0 > 0.f ? (m0 + __log2f(l0)) * 0.69314718055994530942f : -CUDART_INF_F;
+    for (int s = 0; s < kN / 16; ++s)
+      tc::mma_ts(tmem + kColO, pcol + 8 * s, tc::desc_sw128(vb + s * 2048, kHalfBlock, 1024), idO,
+                 (u > 0 || s > 0) ? 1u : 0u);
+    tc::commit(bar + 8 * (B_KV_EMPTY + (u & 1)));
+    tc::commit(bar + 8 * B_PV_DONE);
+    return true;
+  };
+  bool ok = tc::mbar_wait(bar + 8 * B_Q_FULL, 0, abort, p.status, kWaitNs);
+  for (int t = 0; ok && t < ntiles; ++t) {
+    if (!tc::mbar_wait(bar + 8 * (B_KV_FULL + (t & 1)), (t >> 1) & 1, abort, p.status, kWaitNs)) {
+      ok = false;
+      break;
+    }
+    tc::fence_proxy_async();
+    tc::fence_after();
+    const uint32_t qb = base + kOffQ;
+    const uint32_t kb = base + kOffStage + (t & 1) * 2 * kTile;
+#pragma unroll
+    for (int s = 0; s < 8; ++s) {
+      const uint32_t koff = (s >> 2) * kHalfBlock + (s & 3) * 32;
+      tc::mma_ss(tmem + (t & 1) * 128, tc::desc_sw128(qb + koff, 16, 1024),
+                 tc::desc_sw128(kb + koff, 16, 1024), idS, s > 0 ? 1u : 0u);
+    }
+    tc::commit(bar + 8 * (B_S_FULL + (t & 1)));
+    if (t >= 1 && !pv(t - 1)) ok = false;
   }
-  if (r1 < n_rows) {
-    const int qh = it.kv_head * p.gq + r1 % p.gq;
-    __nv_bfloat16* dst = p.o + ((int64_t)qrow1 * p.hq + qh) * kHeadDim + 2 * (lane & 3);
+  if (ok && ntiles > 0) pv(ntiles - 1);
+  // drain: every MMA issued above completes before TMEM is released
+  tc::commit(bar + 8 * B_FINAL);
+  tc::mbar_wait(bar + 8 * B_FINAL, 0, abort, p.status, kWaitNs);
+}
+
+__device__ __forceinline__ void softmax_rows(const ExtParams& p, const ExtItem& it,
+                                             const ExtSeg* segs, int ntiles, uint32_t base,
+                                             uint32_t tmem, volatile int* abort) {
+  const int r = threadIdx.x;  // query row == TMEM lane
+  const int warp = r >> 5;
+  const uint32_t lane_t = tmem + ((uint32_t)(32 * warp) << 16);
+  const uint32_t bar = base + kOffBar;
+  const int n_rows = it.n_tok * p.gq;
+  const bool valid = r < n_rows;
+  int owner = -2, kmax = 0, q_row = 0;
+  if (valid) {
+    const ExtRow e = p.rows[it.row_begin + r / p.gq];
+    owner = e.owner;
+    kmax = e.kmax;
+    q_row = e.q_row;
+  }
+  const float sl2 = p.scale_log2;
+  float m_used = -CUDART_INF_F, l = 0.f;
+  TileIter cur{0, segs[0].k_begin};
+  bool ok = true;
+  for (int t = 0; t < ntiles; ++t) {
+    const int b = t & 1;
+    const bool w_ok = tc::mbar_wait(bar + 8 * (B_S_FULL + b), (t >> 1) & 1, abort, p.status,
+                                    kWaitNs);
+    if (__any_sync(0xffffffffu, !w_ok)) {  // the warp leaves together
+      ok = false;
+      break;
+    }
+    tc::fence_after();
+    const ExtSeg sg = segs[cur.seg];
+    const bool vis = valid && (sg.owner < 0 || sg.owner == owner);
+    const int lim = vis ? min(kmax, sg.k_end) : 0;  // keys at positions >= lim are masked
+    const int n_ok = max(0, min(kN, lim - cur.k0));
+    uint32_t sr[4][32];
 #pragma unroll
-    for (int n = 0; n < 16; ++n)
-      *reinterpret_cast<uint32_t*>(dst + 8 * n) = pack_bf16(o[n][2] * inv1, o[n][3] * inv1);
-    if ((lane & 3) == 0)
-      p.lse[(int64_t)qrow1 * p.hq + qh] =
-          l1 > 0.f ? (m1 + __log2f(l1)) * 0.69314718055994530942f : -CUDART_INF_F;
+    for (int q4 = 0; q4 < 4; ++q4) tc::ld32(lane_t + b * 128 + 32 * q4, sr[q4]);
+    tc::wait_ld();
+    float mx = -CUDART_INF_F;
+#pragma unroll
+    for (int q4 = 0; q4 < 4; ++q4)
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (32 * q4 + j < n_ok) mx = fmaxf(mx, __uint_as_float(sr[q4][j]));
+    const float m_new = n_ok > 0 ? fmaxf(m_used, mx * sl2) : m_used;
+    const bool need = m_new > m_used + 8.f;
+    if (__any_sync(0xffffffffu, need)) {
+      const float alpha = need ? fast_exp2(m_used - m_new) : 1.f;  // exp2(-inf) = 0
+      if (t > 0) {
+        const bool w_ok = tc::mbar_wait(bar + 8 * B_PV_DONE, (t - 1) & 1, abort, p.status,
+                                        kWaitNs);
+        if (__any_sync(0xffffffffu, !w_ok)) {
+          ok = false;
+          break;
+        }
+        tc::fence_after();
+#pragma unroll 1
+        for (int q4 = 0; q4 < 4; ++q4) {
+          uint32_t ov[32];
+          tc::ld32(lane_t + kColO + 32 * q4, ov);
+          tc::wait_ld();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) ov[j] = __float_as_uint(__uint_as_float(ov[j]) * alpha);
+          tc::st32(lane_t + kColO + 32 * q4, ov);
+        }
+        tc::wait_st();
+      }
+      l *= alpha;
+      if (need) m_used = m_new;
+    }
+    float ps = 0.f;
+    uint32_t pk[2][32];
+#pragma unroll
+    for (int q4 = 0; q4 < 4; ++q4)
+#pragma unroll
+      for (int j = 0; j < 32; j += 2) {
+        const int c = 32 * q4 + j;
+        const float p0 = c < n_ok ? fast_exp2(fmaf(__uint_as_float(sr[q4][j]), sl2, -m_used)) : 0.f;
+        const float p1 =
+            c + 1 < n_ok ? fast_exp2(fmaf(__uint_as_float(sr[q4][j + 1]), sl2, -m_used)) : 0.f;
+        ps += p0 + p1;
+        pk[q4 >> 1][(c & 63) >> 1] = pack_bf16(p0, p1);
+      }
+    l += ps;
+    tc::st32(lane_t + kColP + b * 64, pk[0]);
+    tc::st32(lane_t + kColP + b * 64 + 32, pk[1]);
+    tc::wait_st();
+    tc::fence_before();
+    tc::mbar_arrive(bar + 8 * (B_P_FULL + b));
+    tile_next(cur, segs, it.n_seg);
+  }
+  if (!ok || ntiles == 0) return;
+  const bool w_ok = tc::mbar_wait(bar + 8 * B_PV_DONE, (ntiles - 1) & 1, abort, p.status, kWaitNs);
+  if (__any_sync(0xffffffffu, !w_ok)) return;
+  tc::fence_after();
+  const float inv = l > 0.f ? 1.f / l : 0.f;
+  const int qh = it.kv_head * p.gq + (r % p.gq);
+  __nv_bfloat16* dst = p.o + ((int64_t)q_row * p.hq + qh) * kHeadDim;
+#pragma unroll 1
+  for (int q4 = 0; q4 < 4; ++q4) {
+    uint32_t ov[32];
+    tc::ld32(lane_t + kColO + 32 * q4, ov);
+    tc::wait_ld();
+    if (valid) {
+      uint32_t w[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        w[j] = pack_bf16(__uint_as_float(ov[2 * j]) * inv, __uint_as_float(ov[2 * j + 1]) * inv);
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        *reinterpret_cast<uint4*>(dst + 32 * q4 + 8 * j) =
+            make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+    }
+  }
+  if (valid)
+    p.lse[(int64_t)q_row * p.hq + qh] =
+        l > 0.f ? (m_used + __log2f(l)) * 0.69314718055994530942f : -CUDART_INF_F;
+}
+
+__global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(ExtParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023) & ~1023u;
+  uint8_t* sp = smem_raw + (base - raw);
+  const ExtItem it = p.items[blockIdx.x];
+  const int warp = threadIdx.x >> 5;
+  ExtSeg* segs = reinterpret_cast<ExtSeg*>(sp + kOffSegs);
+  volatile int* abort = reinterpret_cast<volatile int*>(sp + kOffAbort);
+  for (int i = threadIdx.x; i < it.n_seg; i += kThreads) segs[i] = p.segs[it.seg_begin + i];
+  if (threadIdx.x == 0) {
+    const uint32_t bar = base + kOffBar;
+    tc::mbar_init(bar + 8 * (B_KV_FULL + 0), kProducers);
+    tc::mbar_init(bar + 8 * (B_KV_FULL + 1), kProducers);
+    tc::mbar_init(bar + 8 * (B_KV_EMPTY + 0), 1);
+    tc::mbar_init(bar + 8 * (B_KV_EMPTY + 1), 1);
+    tc::mbar_init(bar + 8 * B_Q_FULL, kProducers);
+    tc::mbar_init(bar + 8 * (B_S_FULL + 0), 1);
+    tc::mbar_init(bar + 8 * (B_S_FULL + 1), 1);
+    tc::mbar_init(bar + 8 * (B_P_FULL + 0), 128);
+    tc::mbar_init(bar + 8 * (B_P_FULL + 1), 128);
+    tc::mbar_init(bar + 8 * B_PV_DONE, 1);
+    tc::mbar_init(bar + 8 * B_FINAL, 1);
+    *abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 4) tc::alloc(base + kOffTmem, kTmemCols);
+  tc::fence_before();
+  __syncthreads();
+  tc::fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sp + kOffTmem);
+  int ntiles = 0;
+  for (int s = 0; s < it.n_seg; ++s) ntiles += (segs[s].k_end - segs[s].k_begin + kN - 1) / kN;
+
+  if (warp < 4) {
+    softmax_rows(p, it, segs, ntiles, base, tmem, abort);
+  } else if (warp == 4) {
+    if ((threadIdx.x & 31) == 0) mma_issuer(p, ntiles, base, tmem, abort);
+    __syncwarp();
+  } else {
+    producer(p, it, segs, ntiles, base, sp, abort);
+  }
+  tc::fence_before();
+  __syncthreads();
+  if (warp == 4) {
+    tc::fence_after();
+    tc::dealloc(tmem, kTmemCols);
   }
 }
 
@@ -271,7 +375,7 @@ int launch_extend(const rx_kv_desc* d, const PlanHeader* h, const void* k_pool,
                   void* stream) {
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(extend_mma_kernel,
+    cudaError_t e = cudaFuncSetAttribute(extend_tc_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
     if (e != cudaSuccess) return (int)e;
     attr_set = true;
@@ -295,7 +399,7 @@ int launch_extend(const rx_kv_desc* d, const PlanHeader* h, const void* k_pool,
   p.pool_size = d->pool_size;
   p.status = reinterpret_cast<int32_t*>(base + offsetof(PlanHeader, status));
   if (h->n_items > 0)
-    extend_mma_kernel<<<h->n_items, kThreads, kSmem, (cudaStream_t)stream>>>(p);
+    extend_tc_kernel<<<h->n_items, kThreads, kSmem, (cudaStream_t)stream>>>(p);
   return (int)cudaGetLastError();
 }
 
