@@ -9,19 +9,24 @@
 // keys (visible to that member's rows only, causal on its new tokens).  One online softmax runs
 // across all segments, so no partial results leave the CTA.
 //
-// Blackwell tile loop (one CTA per work item, 256 threads, warp-specialised):
-//   warps 5-7  producers: gather the next 128 keys' K and V rows by slot with 16-byte cp.async
-//              into a 2-stage ring laid out as 128-byte-swizzled UMMA tiles; completion is
-//              signalled per stage with cp.async.mbarrier.arrive;
-//   warp 4     MMA issuer (one thread): S = Q K^T with tcgen05.mma (both operands K-major in
+// Blackwell tile loop (one CTA per work item, 256 threads, warp-specialised, 64 keys per step):
+//   warp 4     K producer, warp 5 V producer: gather the keys' 256-byte rows by slot with TMA
+//              (cp.async.bulk.tensor tile::gather4: four pool rows per instruction, 128-byte
+//              swizzle applied by the copy engine) into 6-stage rings laid out as UMMA tiles;
+//              slot indices are fetched two steps ahead; a stage completes on its mbarrier's
+//              transaction count.
+//   warp 6     MMA issuer (one thread): S = Q K^T with tcgen05.mma (both operands K-major in
 //              shared memory, fp32 accumulator in TMEM, double-buffered), then O += P V with P
-//              read from TMEM and V as an MN-major shared-memory operand;
-//   warps 0-3  softmax: thread r owns query row r (TMEM lane r): tcgen05.ld of its S row, masks,
-//              online max / sum in base 2 (the running max is only moved -- and O in TMEM rescaled
-//              -- when it grows by more than 2^8), P = exp2(.) packed to bf16 and written to its own
-//              TMEM columns with tcgen05.st for the PV MMA; finally O / l and the LSE.
+//              read from TMEM and V as an MN-major shared-memory operand.
+//   warps 0-3  softmax: thread r owns query row r (TMEM lane r) and copies it into the Q tile
+//              first; per step: tcgen05.ld of its S row, masks,
+//              online max / sum in base 2 (the running max is only moved -- and O in TMEM
+//              rescaled -- when it grows by more than 2^8), P = exp2(.) packed to bf16 and written
+//              to its own TMEM columns with tcgen05.st for the PV MMA; finally O / l and the LSE.
 // Every mbarrier wait is bounded (globaltimer); a timeout records RX_ERR_TIMEOUT in the
 // workspace status word and every role leaves its loop.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <math_constants.h>
 
@@ -47,28 +52,48 @@ struct ExtParams {
   const ExtSeg* segs;
   int64_t pool_size;
   int32_t* status;
+  int32_t oob_row;  // a row index past the end of the pool's [pool_size * Hkv, 128] view
 };
 
-constexpr int kThreads = 256;
-constexpr int kProducers = 96;          // warps 5..7
-constexpr int kN = 128;                 // keys per tile
-constexpr int kStages = 2;
-constexpr int kMaxSegs = 1 + 128;
-constexpr int kHalfBlock = 128 * 128;   // one 64-column half of a 128-row tile: 16 KiB
-constexpr int kTile = 2 * kHalfBlock;   // 128 rows x 128 bf16: 32 KiB
+constexpr int kThreads = 256;           // warps 0-3 softmax, 4 K producer, 5 V producer, 6 MMA
+constexpr int kN = 64;                  // keys per step
+constexpr int kStages = 6;              // K ring and V ring depth
+constexpr int kQHalf = 128 * 128;       // one 64-column half of the 128-row query tile: 16 KiB
+constexpr int kKVHalf = kN * 128;       // one 64-column half of a 64-key K or V tile: 8 KiB
+constexpr int kKVTile = 2 * kKVHalf;    // 16 KiB
 constexpr int kOffQ = 0;
-constexpr int kOffStage = kTile;                        // stage s: K at +s*2*kTile, V after it
-constexpr int kOffSlots = kOffStage + kStages * 2 * kTile;
-constexpr int kOffSegs = kOffSlots + kStages * kN * 4;
-constexpr int kOffBar = kOffSegs + kMaxSegs * 16;
-enum { B_KV_FULL = 0, B_KV_EMPTY = 2, B_Q_FULL = 4, B_S_FULL = 5, B_P_FULL = 7, B_PV_DONE = 9,
-       B_FINAL = 10, B_COUNT = 11 };
+constexpr int kOffK = 2 * kQHalf;
+constexpr int kOffV = kOffK + kStages * kKVTile;
+constexpr int kOffBar = kOffV + kStages * kKVTile;
+// Barriers (each waiter is at most one phase behind the barrier it tests):
+//   K_FULL[k] / V_FULL[k]   step in ring stage k landed (producer warp, 32 arrivals)
+//   K_FREE[k]  S(t) = Q K(t)^T complete, K stage free           (commit after S(t))
+//   S_FULL[b]  S(t) readable by the softmax, b = t & 1          (commit after S(t))
+//   V_FREE[k]  O += P(u) V(u) complete, V stage free             (commit after PV(u))
+//   PV_DONE    PV(u) complete for u < last, O stable for a rescale (commit after PV(u))
+//   PV_LAST    the last PV complete, O final for the epilogue
+//   P_FULL[b]  P(t) in TMEM (128 softmax threads)
+// (a tcgen05.commit tracks every MMA the thread issued before it, so several commits may follow
+// one batch of MMAs)
+enum {
+  B_K_FULL = 0,
+  B_K_FREE = B_K_FULL + kStages,
+  B_V_FULL = B_K_FREE + kStages,
+  B_V_FREE = B_V_FULL + kStages,
+  B_S_FULL = B_V_FREE + kStages,
+  B_P_FULL = B_S_FULL + 2,
+  B_Q_FULL = B_P_FULL + 2,
+  B_PV_DONE,
+  B_PV_LAST,
+  B_COUNT
+};
 constexpr int kOffTmem = kOffBar + B_COUNT * 8;
 constexpr int kOffAbort = kOffTmem + 8;
 constexpr size_t kSmem = 1024 + kOffAbort + 16;
-constexpr uint32_t kTmemCols = 512;     // S0 [0,128), S1 [128,256), O [256,384), P0, P1 64 each
-constexpr uint32_t kColO = 256;
-constexpr uint32_t kColP = 384;
+// TMEM columns: S0 [0,64), S1 [64,128), O [128,256), P0 [256,288), P1 [288,320)
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColO = 128;
+constexpr uint32_t kColP = 256;
 constexpr uint64_t kWaitNs = 2000000000ull;
 
 static_assert(kSmem <= 227 * 1024, "shared memory budget");
@@ -77,6 +102,7 @@ struct TileIter {
   int seg, k0;
 };
 __device__ __forceinline__ void tile_next(TileIter& c, const ExtSeg* segs, int n_seg) {
+  if (c.seg >= n_seg) return;  // already past the last segment: never read beyond the item
   c.k0 += kN;
   if (c.k0 >= segs[c.seg].k_end) {
     ++c.seg;
@@ -84,76 +110,107 @@ __device__ __forceinline__ void tile_next(TileIter& c, const ExtSeg* segs, int n
   }
 }
 
-// byte offset of 16-byte chunk c (0..15) of row r in a K-major 128-row tile (two SW128 halves)
-__device__ __forceinline__ uint32_t tile_off(int r, int c) {
-  return (uint32_t)((c >> 3) * kHalfBlock + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+// Byte offset of 16-byte chunk c (0..15) of row r in a K-major tile stored as two 128-byte-
+// swizzled halves (d 0..63, d 64..127) of `half` bytes each.
+__device__ __forceinline__ uint32_t tile_off(int r, int c, int half) {
+  return (uint32_t)((c >> 3) * half + r * 128 + (((c & 7) ^ (r & 7)) << 4));
 }
 
-// Named barrier over `n` threads that also ORs a predicate across them.
-__device__ __forceinline__ bool bar_any(int id, int n, bool pred) {
-  uint32_t r;
+// Raw table entry for key position k0 + key of segment sg (-1 past the segment).  No test on the
+// loaded value here, so the load stays in flight until the slot is used; check_slot validates it.
+__device__ __forceinline__ int fetch_slot(const ExtParams& p, const ExtSeg& sg, int k0, int key) {
+  const int kpos = k0 + key;
+  return kpos < sg.k_end ? __ldg(p.req_to_token + (int64_t)sg.kv_row * p.stride + kpos) : -1;
+}
+
+// -1 stays -1 (nothing to load); an entry outside the pool flags RX_ERR_RANGE and is not read.
+__device__ __forceinline__ int check_slot(const ExtParams& p, int s) {
+  if (s >= p.pool_size || s < -1) {
+    atomicCAS(p.status, 0, (int)RX_ERR_RANGE);
+    return -1;
+  }
+  return s;
+}
+
+// TMA gather of four pool rows (one 64-column half each) into consecutive 128-byte rows of a
+// 128-byte-swizzled tile; completion is counted in bytes on `mbar`.
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map, int col, int r0,
+                                            int r1, int r2, int r3, uint32_t mbar) {
   asm volatile(
-      "{\n.reg .pred p, q;\nsetp.ne.u32 p, %1, 0;\nbar.red.or.pred q, %2, %3, p;\n"
-      "selp.u32 %0, 1, 0, q;\n}\n"
-      : "=r"(r)
-      : "r"((uint32_t)pred), "r"(id), "r"(n)
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+      "l"(map), "r"(col), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(mbar)
       : "memory");
-  return r != 0;
 }
 
-__device__ __forceinline__ void cp_async_mbar_arrive(uint32_t mbar) {
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(mbar) : "memory");
+__device__ __forceinline__ void mbar_expect_tx(uint32_t mbar, uint32_t bytes) {
+  asm volatile("{\n.reg .b64 st;\nmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n}\n" ::"r"(
+                   mbar),
+               "r"(bytes)
+               : "memory");
 }
+
+// Producer warp of one operand (K or V).  The pool is viewed by the tensor map as rows of 128
+// bf16 (row = slot * Hkv + head).  Lane j fetches the table entries of keys j and j + 32 two
+// steps ahead; per step lane j then gathers keys 4 (j % 16) .. 4 (j % 16) + 3, half j / 16 of
+// their 256-byte rows, with one tile::gather4 (32 gathers = the 64 keys' K or V).  Keys past the
+// segment (or flagged entries) read a row past the end of the map, which the TMA fills with zeros.
+// The step loop is unrolled by three so the prefetched entries rotate through registers by
+// position: copying a register whose load is still in flight would wait for the load.
+struct SlotPair {
+  int lo, hi;  // entries of keys lane and lane + 32
+};
 
 __device__ __forceinline__ void producer(const ExtParams& p, const ExtItem& it,
                                          const ExtSeg* segs, int ntiles, uint32_t base,
-                                         uint8_t* sp, volatile int* abort) {
-  const int ptid = threadIdx.x - 160;
-  const int n_rows = it.n_tok * p.gq;
-  // query tile
-  for (int i = ptid; i < 128 * 16; i += kProducers) {
-    const int r = i >> 4, c = i & 15;
-    const bool ok = r < n_rows;
-    const __nv_bfloat16* src =
-        ok ? p.q + ((int64_t)p.rows[it.row_begin + r / p.gq].q_row * p.hq + it.kv_head * p.gq +
-                    r % p.gq) * kHeadDim + c * 8
-           : p.q;
-    cp_async16(base + kOffQ + tile_off(r, c), src, ok);
-  }
-  cp_async_mbar_arrive(base + kOffBar + 8 * B_Q_FULL);
-  TileIter cur{0, segs[0].k_begin};
-  for (int t = 0; t < ntiles; ++t) {
-    const int st = t & 1;
-    const bool waited = t < kStages ||
-        tc::mbar_wait(base + kOffBar + 8 * (B_KV_EMPTY + st), ((t >> 1) - 1) & 1, abort,
-                      p.status, kWaitNs);
-    const ExtSeg sg = segs[cur.seg];
-    int32_t* slots = reinterpret_cast<int32_t*>(sp + kOffSlots) + st * kN;
-    const int32_t* r2t = p.req_to_token + (int64_t)sg.kv_row * p.stride;
-    for (int k = ptid; waited && k < kN; k += kProducers) {
-      const int kpos = cur.k0 + k;
-      int s = kpos < sg.k_end ? __ldg(r2t + kpos) : -1;
-      if (kpos < sg.k_end && (s < 0 || s >= p.pool_size)) {  // outside the pool: flag, skip
-        atomicCAS(p.status, 0, (int)RX_ERR_RANGE);
-        s = -1;
-      }
-      slots[k] = s;
+                                         const CUtensorMap* map, uint32_t ring, int b_full,
+                                         int b_free, volatile int* abort) {
+  const int lane = threadIdx.x & 31;
+  const int g = lane & 15, h = lane >> 4;
+  const uint32_t bar = base + kOffBar;
+  TileIter ahead{0, segs[0].k_begin};
+  auto fetch_next = [&](SlotPair& sp) {  // entries of the step `ahead` points at, then advance
+    sp.lo = fetch_slot(p, segs[ahead.seg], ahead.k0, lane);
+    sp.hi = fetch_slot(p, segs[ahead.seg], ahead.k0, 32 + lane);
+    tile_next(ahead, segs, it.n_seg);
+  };
+  SlotPair s0{-1, -1}, s1{-1, -1}, s2{-1, -1};
+  if (ntiles > 0) fetch_next(s0);
+  if (ntiles > 1) fetch_next(s1);
+  bool ok = true;
+  // one step: prefetch step t + 2 into `later`, wait for the stage, gather step t from `cur`
+  auto step = [&](int t, const SlotPair& cur, SlotPair& later) {
+    if (!ok || t >= ntiles) return;
+    if (t + 2 < ntiles) fetch_next(later);
+    const int st = t % kStages;
+    const bool waited = t < kStages || tc::mbar_wait(bar + 8 * (b_free + st),
+                                                     (t / kStages - 1) & 1, abort, p.status,
+                                                     kWaitNs);
+    if (__any_sync(0xffffffffu, !waited)) {  // the warp leaves together
+      ok = false;
+      return;
     }
-    // slots visible to all producers; leave together if any of them gave up waiting
-    if (bar_any(1, kProducers, !waited || *abort)) break;
-    const uint32_t kb = base + kOffStage + st * 2 * kTile;
-    for (int i = ptid; i < kN * 16; i += kProducers) {
-      const int key = i >> 4, c = i & 15;
-      const int s = slots[key];
-      const int64_t off = s >= 0 ? ((int64_t)s * p.hkv + it.kv_head) * kHeadDim + c * 8 : 0;
-      const uint32_t so = tile_off(key, c);
-      cp_async16(kb + so, p.k_pool + off, s >= 0);
-      cp_async16(kb + kTile + so, p.v_pool + off, s >= 0);
+    const int v0 = check_slot(p, cur.lo), v1 = check_slot(p, cur.hi);
+    const int row0 = v0 >= 0 ? v0 * p.hkv + it.kv_head : p.oob_row;
+    const int row1 = v1 >= 0 ? v1 * p.hkv + it.kv_head : p.oob_row;
+    int r[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int key = 4 * g + j;  // lane-dependent: shuffle both halves, select after
+      const int x0 = __shfl_sync(0xffffffffu, row0, key & 31);
+      const int x1 = __shfl_sync(0xffffffffu, row1, key & 31);
+      r[j] = key < 32 ? x0 : x1;
     }
-    cp_async_mbar_arrive(base + kOffBar + 8 * (B_KV_FULL + st));
-    tile_next(cur, segs, it.n_seg);
+    if (lane == 0) mbar_expect_tx(bar + 8 * (b_full + st), kN * kHeadDim * 2);
+    __syncwarp();
+    tma_gather4(ring + st * kKVTile + h * kKVHalf + g * 512, map, 64 * h, r[0], r[1], r[2], r[3],
+                bar + 8 * (b_full + st));
+  };
+  for (int t = 0; ok && t < ntiles; t += 3) {
+    step(t, s0, s2);
+    step(t + 1, s1, s0);
+    step(t + 2, s2, s1);
   }
-  cp_async_wait<0>();
 }
 
 __device__ __forceinline__ void mma_issuer(const ExtParams& p, int ntiles, uint32_t base,
@@ -161,43 +218,92 @@ __device__ __forceinline__ void mma_issuer(const ExtParams& p, int ntiles, uint3
   constexpr uint32_t idS = tc::idesc_bf16(128, kN, false, false);
   constexpr uint32_t idO = tc::idesc_bf16(128, 128, false, true);
   const uint32_t bar = base + kOffBar;
+  uint32_t last_bar = 0, last_parity = 0;  // the most recent commit, drained before exit
   auto pv = [&](int u) -> bool {
+    const int vs = u % kStages;
     if (!tc::mbar_wait(bar + 8 * (B_P_FULL + (u & 1)), (u >> 1) & 1, abort, p.status, kWaitNs))
       return false;
+    if (!tc::mbar_wait(bar + 8 * (B_V_FULL + vs), (u / kStages) & 1, abort, p.status, kWaitNs))
+      return false;
     tc::fence_after();
-    const uint32_t vb = base + kOffStage + (u & 1) * 2 * kTile + kTile;
-    const uint32_t pcol = tmem + kColP + (u & 1) * 64;
+    const uint32_t vb = base + kOffV + vs * kKVTile;
+    const uint32_t pcol = tmem + kColP + (u & 1) * (kN / 2);
 #pragma unroll
     for (int s = 0; s < kN / 16; ++s)
-      tc::mma_ts(tmem + kColO, pcol + 8 * s, tc::desc_sw128(vb + s * 2048, kHalfBlock, 1024), idO,
+      tc::mma_ts(tmem + kColO, pcol + 8 * s, tc::desc_sw128(vb + s * 2048, kKVHalf, 1024), idO,
                  (u > 0 || s > 0) ? 1u : 0u);
-    tc::commit(bar + 8 * (B_KV_EMPTY + (u & 1)));
-    tc::commit(bar + 8 * B_PV_DONE);
+    const bool last = u == ntiles - 1;
+    tc::commit(bar + 8 * (B_V_FREE + vs));
+    tc::commit(bar + 8 * (last ? B_PV_LAST : B_PV_DONE));
+    last_bar = bar + 8 * (last ? B_PV_LAST : B_PV_DONE);
+    last_parity = last ? 0 : (u & 1);
     return true;
   };
   bool ok = tc::mbar_wait(bar + 8 * B_Q_FULL, 0, abort, p.status, kWaitNs);
   for (int t = 0; ok && t < ntiles; ++t) {
-    if (!tc::mbar_wait(bar + 8 * (B_KV_FULL + (t & 1)), (t >> 1) & 1, abort, p.status, kWaitNs)) {
+    const int ks = t % kStages;
+    if (!tc::mbar_wait(bar + 8 * (B_K_FULL + ks), (t / kStages) & 1, abort, p.status, kWaitNs)) {
       ok = false;
       break;
     }
-    tc::fence_proxy_async();
     tc::fence_after();
     const uint32_t qb = base + kOffQ;
-    const uint32_t kb = base + kOffStage + (t & 1) * 2 * kTile;
+    const uint32_t kb = base + kOffK + ks * kKVTile;
 #pragma unroll
     for (int s = 0; s < 8; ++s) {
-      const uint32_t koff = (s >> 2) * kHalfBlock + (s & 3) * 32;
-      tc::mma_ss(tmem + (t & 1) * 128, tc::desc_sw128(qb + koff, 16, 1024),
-                 tc::desc_sw128(kb + koff, 16, 1024), idS, s > 0 ? 1u : 0u);
+      const uint32_t koff = (s & 3) * 32;
+      tc::mma_ss(tmem + (t & 1) * kN, tc::desc_sw128(qb + (s >> 2) * kQHalf + koff, 16, 1024),
+                 tc::desc_sw128(kb + (s >> 2) * kKVHalf + koff, 16, 1024), idS, s > 0 ? 1u : 0u);
     }
+    tc::commit(bar + 8 * (B_K_FREE + ks));
     tc::commit(bar + 8 * (B_S_FULL + (t & 1)));
+    last_bar = bar + 8 * (B_S_FULL + (t & 1));
+    last_parity = (t >> 1) & 1;
     if (t >= 1 && !pv(t - 1)) ok = false;
   }
   if (ok && ntiles > 0) pv(ntiles - 1);
-  // drain: every MMA issued above completes before TMEM is released
-  tc::commit(bar + 8 * B_FINAL);
-  tc::mbar_wait(bar + 8 * B_FINAL, 0, abort, p.status, kWaitNs);
+  // drain: the MMAs issued above complete before TMEM is released
+  if (last_bar) tc::mbar_wait(last_bar, last_parity, abort, p.status, kWaitNs);
+}
+
+// Row maximum of the first n_ok raw scores (all kN when !MASKED), as a tree of independent
+// maxima so the chain stays short.
+template <bool MASKED>
+__device__ __forceinline__ float row_max(const uint32_t (&sr)[2][32], int n_ok) {
+  float m[8];
+#pragma unroll
+  for (int a = 0; a < 8; ++a) m[a] = -CUDART_INF_F;
+#pragma unroll
+  for (int q2 = 0; q2 < 2; ++q2)
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (!MASKED || 32 * q2 + j < n_ok) m[j & 7] = fmaxf(m[j & 7], __uint_as_float(sr[q2][j]));
+#pragma unroll
+  for (int a = 0; a < 4; ++a) m[a] = fmaxf(m[a], m[a + 4]);
+  return fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3]));
+}
+
+// p_j = 2^(s_j * scale_log2 - m) for the first n_ok keys (0 beyond), packed to bf16 pairs in pk;
+// returns the sum of the p_j (four independent partial sums).
+template <bool MASKED>
+__device__ __forceinline__ float row_exp(const uint32_t (&sr)[2][32], int n_ok, float sl2,
+                                         float m, uint32_t (&pk)[32]) {
+  float ps[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int q2 = 0; q2 < 2; ++q2)
+#pragma unroll
+    for (int j = 0; j < 32; j += 2) {
+      const int c = 32 * q2 + j;
+      float p0 = fast_exp2(fmaf(__uint_as_float(sr[q2][j]), sl2, -m));
+      float p1 = fast_exp2(fmaf(__uint_as_float(sr[q2][j + 1]), sl2, -m));
+      if (MASKED) {
+        p0 = c < n_ok ? p0 : 0.f;
+        p1 = c + 1 < n_ok ? p1 : 0.f;
+      }
+      ps[(j >> 1) & 3] += p0 + p1;
+      pk[c >> 1] = pack_bf16(p0, p1);
+    }
+  return (ps[0] + ps[1]) + (ps[2] + ps[3]);
 }
 
 __device__ __forceinline__ void softmax_rows(const ExtParams& p, const ExtItem& it,
@@ -216,6 +322,18 @@ __device__ __forceinline__ void softmax_rows(const ExtParams& p, const ExtItem& 
     kmax = e.kmax;
     q_row = e.q_row;
   }
+  {
+    // query row r -> the Q tile (16 chunks of 16 bytes), then visible to the tensor core
+    const int qh = it.kv_head * p.gq + (r % p.gq);
+    const __nv_bfloat16* src = p.q + ((int64_t)q_row * p.hq + qh) * kHeadDim;
+#pragma unroll
+    for (int c = 0; c < 16; ++c)
+      cp_async16(base + kOffQ + tile_off(r, c, kQHalf), valid ? src + c * 8 : p.q, valid);
+    cp_async_commit();
+    cp_async_wait<0>();
+    tc::fence_proxy_async();
+    tc::mbar_arrive(bar + 8 * B_Q_FULL);
+  }
   const float sl2 = p.scale_log2;
   float m_used = -CUDART_INF_F, l = 0.f;
   TileIter cur{0, segs[0].k_begin};
@@ -233,24 +351,22 @@ __device__ __forceinline__ void softmax_rows(const ExtParams& p, const ExtItem& 
     const bool vis = valid && (sg.owner < 0 || sg.owner == owner);
     const int lim = vis ? min(kmax, sg.k_end) : 0;  // keys at positions >= lim are masked
     const int n_ok = max(0, min(kN, lim - cur.k0));
-    uint32_t sr[4][32];
-#pragma unroll
-    for (int q4 = 0; q4 < 4; ++q4) tc::ld32(lane_t + b * 128 + 32 * q4, sr[q4]);
+    uint32_t sr[2][32];
+    tc::ld32(lane_t + b * kN, sr[0]);
+    tc::ld32(lane_t + b * kN + 32, sr[1]);
     tc::wait_ld();
-    float mx = -CUDART_INF_F;
-#pragma unroll
-    for (int q4 = 0; q4 < 4; ++q4)
-#pragma unroll
-      for (int j = 0; j < 32; ++j)
-        if (32 * q4 + j < n_ok) mx = fmaxf(mx, __uint_as_float(sr[q4][j]));
+    // the unmasked path only when the whole warp takes it: the tcgen05.ld/st around these
+    // loops are warp-collective and must not be reached from diverged paths
+    const bool full = __all_sync(0xffffffffu, n_ok == kN);
+    const float mx = full ? row_max<false>(sr, n_ok) : row_max<true>(sr, n_ok);
     const float m_new = n_ok > 0 ? fmaxf(m_used, mx * sl2) : m_used;
     const bool need = m_new > m_used + 8.f;
     if (__any_sync(0xffffffffu, need)) {
       const float alpha = need ? fast_exp2(m_used - m_new) : 1.f;  // exp2(-inf) = 0
       if (t > 0) {
-        const bool w_ok = tc::mbar_wait(bar + 8 * B_PV_DONE, (t - 1) & 1, abort, p.status,
-                                        kWaitNs);
-        if (__any_sync(0xffffffffu, !w_ok)) {
+        const bool w2 = tc::mbar_wait(bar + 8 * B_PV_DONE, (t - 1) & 1, abort, p.status,
+                                      kWaitNs);
+        if (__any_sync(0xffffffffu, !w2)) {
           ok = false;
           break;
         }
@@ -269,29 +385,18 @@ __device__ __forceinline__ void softmax_rows(const ExtParams& p, const ExtItem& 
       l *= alpha;
       if (need) m_used = m_new;
     }
-    float ps = 0.f;
-    uint32_t pk[2][32];
-#pragma unroll
-    for (int q4 = 0; q4 < 4; ++q4)
-#pragma unroll
-      for (int j = 0; j < 32; j += 2) {
-        const int c = 32 * q4 + j;
-        const float p0 = c < n_ok ? fast_exp2(fmaf(__uint_as_float(sr[q4][j]), sl2, -m_used)) : 0.f;
-        const float p1 =
-            c + 1 < n_ok ? fast_exp2(fmaf(__uint_as_float(sr[q4][j + 1]), sl2, -m_used)) : 0.f;
-        ps += p0 + p1;
-        pk[q4 >> 1][(c & 63) >> 1] = pack_bf16(p0, p1);
-      }
+    uint32_t pk[32];
+    const float ps = full ? row_exp<false>(sr, n_ok, sl2, m_used, pk)
+                          : row_exp<true>(sr, n_ok, sl2, m_used, pk);
     l += ps;
-    tc::st32(lane_t + kColP + b * 64, pk[0]);
-    tc::st32(lane_t + kColP + b * 64 + 32, pk[1]);
+    tc::st32(lane_t + kColP + b * (kN / 2), pk);
     tc::wait_st();
     tc::fence_before();
     tc::mbar_arrive(bar + 8 * (B_P_FULL + b));
     tile_next(cur, segs, it.n_seg);
   }
   if (!ok || ntiles == 0) return;
-  const bool w_ok = tc::mbar_wait(bar + 8 * B_PV_DONE, (ntiles - 1) & 1, abort, p.status, kWaitNs);
+  const bool w_ok = tc::mbar_wait(bar + 8 * B_PV_LAST, 0, abort, p.status, kWaitNs);
   if (__any_sync(0xffffffffu, !w_ok)) return;
   tc::fence_after();
   const float inv = l > 0.f ? 1.f / l : 0.f;
@@ -318,33 +423,36 @@ __device__ __forceinline__ void softmax_rows(const ExtParams& p, const ExtItem& 
         l > 0.f ? (m_used + __log2f(l)) * 0.69314718055994530942f : -CUDART_INF_F;
 }
 
-__global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(ExtParams p) {
+__global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(ExtParams p,
+                                                                const __grid_constant__ CUtensorMap k_map,
+                                                                const __grid_constant__ CUtensorMap v_map) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023) & ~1023u;
   uint8_t* sp = smem_raw + (base - raw);
   const ExtItem it = p.items[blockIdx.x];
   const int warp = threadIdx.x >> 5;
-  ExtSeg* segs = reinterpret_cast<ExtSeg*>(sp + kOffSegs);
+  const ExtSeg* segs = p.segs + it.seg_begin;  // small, read through the L1 by every role
   volatile int* abort = reinterpret_cast<volatile int*>(sp + kOffAbort);
-  for (int i = threadIdx.x; i < it.n_seg; i += kThreads) segs[i] = p.segs[it.seg_begin + i];
   if (threadIdx.x == 0) {
     const uint32_t bar = base + kOffBar;
-    tc::mbar_init(bar + 8 * (B_KV_FULL + 0), kProducers);
-    tc::mbar_init(bar + 8 * (B_KV_FULL + 1), kProducers);
-    tc::mbar_init(bar + 8 * (B_KV_EMPTY + 0), 1);
-    tc::mbar_init(bar + 8 * (B_KV_EMPTY + 1), 1);
-    tc::mbar_init(bar + 8 * B_Q_FULL, kProducers);
+    for (int i = 0; i < kStages; ++i) {
+      tc::mbar_init(bar + 8 * (B_K_FULL + i), 1);
+      tc::mbar_init(bar + 8 * (B_K_FREE + i), 1);
+      tc::mbar_init(bar + 8 * (B_V_FULL + i), 1);
+      tc::mbar_init(bar + 8 * (B_V_FREE + i), 1);
+    }
     tc::mbar_init(bar + 8 * (B_S_FULL + 0), 1);
     tc::mbar_init(bar + 8 * (B_S_FULL + 1), 1);
     tc::mbar_init(bar + 8 * (B_P_FULL + 0), 128);
     tc::mbar_init(bar + 8 * (B_P_FULL + 1), 128);
+    tc::mbar_init(bar + 8 * B_Q_FULL, 128);
     tc::mbar_init(bar + 8 * B_PV_DONE, 1);
-    tc::mbar_init(bar + 8 * B_FINAL, 1);
+    tc::mbar_init(bar + 8 * B_PV_LAST, 1);
     *abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (warp == 4) tc::alloc(base + kOffTmem, kTmemCols);
+  if (warp == 6) tc::alloc(base + kOffTmem, kTmemCols);
   tc::fence_before();
   __syncthreads();
   tc::fence_after();
@@ -354,18 +462,45 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(ExtParams p) {
 
   if (warp < 4) {
     softmax_rows(p, it, segs, ntiles, base, tmem, abort);
-  } else if (warp == 4) {
+  } else if (warp == 6) {
     if ((threadIdx.x & 31) == 0) mma_issuer(p, ntiles, base, tmem, abort);
     __syncwarp();
-  } else {
-    producer(p, it, segs, ntiles, base, sp, abort);
+  } else if (warp == 4) {
+    producer(p, it, segs, ntiles, base, &k_map, base + kOffK, B_K_FULL, B_K_FREE, abort);
+  } else if (warp == 5) {
+    producer(p, it, segs, ntiles, base, &v_map, base + kOffV, B_V_FULL, B_V_FREE, abort);
   }
   tc::fence_before();
   __syncthreads();
-  if (warp == 4) {
+  if (warp == 6) {
     tc::fence_after();
     tc::dealloc(tmem, kTmemCols);
   }
+}
+
+// Tensor map viewing a pool as [pool_size * num_kv_heads rows, 128 bf16 columns] (row stride
+// 256 bytes), boxes of 64 columns x 1 row, 128-byte swizzle: the unit of tile::gather4.
+int make_pool_map(CUtensorMap* map, const void* pool, const rx_kv_desc* d) {
+  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  if (!encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                     cudaEnableDefault, &q);
+    if (e != cudaSuccess) return (int)e;
+    if (!fn || q != cudaDriverEntryPointSuccess) return (int)cudaErrorNotSupported;
+    encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  const cuuint64_t dims[2] = {(cuuint64_t)kHeadDim,
+                              (cuuint64_t)d->pool_size * (cuuint64_t)d->num_kv_heads};
+  const cuuint64_t strides[1] = {(cuuint64_t)kHeadDim * 2};
+  const cuuint32_t box[2] = {64, 1};
+  const cuuint32_t es[2] = {1, 1};
+  const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(pool), dims,
+                            strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? 0 : (int)cudaErrorInvalidValue;
 }
 
 }  // namespace
@@ -398,8 +533,13 @@ int launch_extend(const rx_kv_desc* d, const PlanHeader* h, const void* k_pool,
   p.segs = reinterpret_cast<const ExtSeg*>(base + h->off_segs);
   p.pool_size = d->pool_size;
   p.status = reinterpret_cast<int32_t*>(base + offsetof(PlanHeader, status));
-  if (h->n_items > 0)
-    extend_tc_kernel<<<h->n_items, kThreads, kSmem, (cudaStream_t)stream>>>(p);
+  if (h->n_items == 0) return 0;
+  CUtensorMap k_map, v_map;
+  int e = make_pool_map(&k_map, k_pool, d);
+  if (!e) e = make_pool_map(&v_map, v_pool, d);
+  if (e) return e;
+  p.oob_row = (int32_t)(d->pool_size * d->num_kv_heads);
+  extend_tc_kernel<<<h->n_items, kThreads, kSmem, (cudaStream_t)stream>>>(p, k_map, v_map);
   return (int)cudaGetLastError();
 }
 

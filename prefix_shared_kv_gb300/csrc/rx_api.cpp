@@ -380,7 +380,7 @@ rx_status rx_decode_attn(const rx_plan* plan, const rx_kv_desc* desc, const void
 // tiles of 128 / gq tokens (128 query rows per KV head).  A tile's segments: the shared prefix
 // (read from the first member's row, visible to all rows) and, per member present, its keys from
 // the group prefix up to its last row's causal limit.  Ungrouped requests get tiles of their own.
-// One item per (tile, KV head), launched longest first.
+// One item per (tile, KV head).
 // ---------------------------------------------------------------------------------------------
 rx_status rx_extend_plan(rx_plan* plan, const rx_kv_desc* desc, int32_t batch,
                          const int32_t* req_idx, const int32_t* prefix_len,
@@ -424,10 +424,15 @@ rx_status rx_extend_plan(rx_plan* plan, const rx_kv_desc* desc, int32_t batch,
     int row_begin, n_tok, seg_begin, n_seg;
     double cost;
   };
-  std::vector<Tile> tiles;
+  // A unit is a group (all its tiles read the same prefix KV) or a lone request.
+  struct Unit {
+    std::vector<Tile> tiles;
+    double cost = 0;
+  };
+  std::vector<Unit> units;
 
-  auto emit_tiles = [&](const std::vector<int>& reqs, int gp) {
-    // token list of the requests, member after member
+  auto emit_unit = [&](const std::vector<int>& reqs, int gp) {
+    Unit un;
     const int first_row = (int)rows.size();
     for (int r : reqs)
       for (int i = 0; i < extend_len[r]; ++i)
@@ -448,13 +453,17 @@ rx_status rx_extend_plan(rx_plan* plan, const rx_kv_desc* desc, int32_t batch,
         const int kend = rows[first_row + t0 + j].kmax;  // last row's causal limit
         if (kend > gp) {
           segs.push_back({req_idx[owner], gp, kend, owner});
-          tl.cost += (double)(kend - gp) * (j - i + 1) / nt;
+          tl.cost += (double)(kend - gp);
         }
         i = j + 1;
       }
       tl.n_seg = (int)segs.size() - tl.seg_begin;
-      tiles.push_back(tl);
+      un.cost += tl.cost;
+      un.tiles.push_back(tl);
     }
+    std::stable_sort(un.tiles.begin(), un.tiles.end(),
+                     [](const Tile& a, const Tile& b) { return a.cost > b.cost; });
+    units.push_back(std::move(un));
   };
 
   std::vector<std::vector<int>> members(num_groups);
@@ -463,25 +472,26 @@ rx_status rx_extend_plan(rx_plan* plan, const rx_kv_desc* desc, int32_t batch,
   for (int g = 0; g < num_groups; ++g) {
     if (members[g].empty()) continue;
     if (group_prefix_len[g] > 0) {
-      emit_tiles(members[g], group_prefix_len[g]);
+      emit_unit(members[g], group_prefix_len[g]);
     } else {
-      for (int b : members[g]) emit_tiles(std::vector<int>{b}, 0);
+      for (int b : members[g]) emit_unit(std::vector<int>{b}, 0);
     }
   }
   for (int b = 0; b < batch; ++b)
-    if (grp[b] < 0 && extend_len[b] > 0) emit_tiles(std::vector<int>{b}, 0);
+    if (grp[b] < 0 && extend_len[b] > 0) emit_unit(std::vector<int>{b}, 0);
 
-  std::vector<size_t> order(tiles.size());
+  // Launch order: largest unit first (longest-processing-time first across units); inside a
+  // unit, KV head outer and tiles inner, so the tiles that read the same prefix K/V of one head
+  // run in the same wave and hit in L2.
+  std::vector<size_t> order(units.size());
   std::iota(order.begin(), order.end(), 0);
   std::stable_sort(order.begin(), order.end(),
-                   [&](size_t a, size_t b) { return tiles[a].cost > tiles[b].cost; });
+                   [&](size_t a, size_t b) { return units[a].cost > units[b].cost; });
   std::vector<ExtItem> items;
-  items.reserve(tiles.size() * hkv);
   for (size_t k : order)
-    for (int h = 0; h < hkv; ++h) {
-      const Tile& t = tiles[k];
-      items.push_back({t.row_begin, t.n_tok, t.seg_begin, t.n_seg, h, {0, 0, 0}});
-    }
+    for (int h = 0; h < hkv; ++h)
+      for (const Tile& t : units[k].tiles)
+        items.push_back({t.row_begin, t.n_tok, t.seg_begin, t.n_seg, h, {0, 0, 0}});
   if (items.size() > (size_t)INT32_MAX) return fail(RX_ERR_RANGE, "plan too large");
 
   PlanHeader h;
@@ -516,6 +526,8 @@ rx_status rx_extend_attn(const rx_plan* plan, const rx_kv_desc* desc, const void
   rx_status st = check_plan_use(plan, 1, desc, k_pool, v_pool, q, o, lse, workspace,
                                 workspace_bytes);
   if (st) return st;
+  if (desc->pool_size * desc->num_kv_heads >= (int64_t)INT32_MAX)
+    return fail(RX_ERR_UNSUPPORTED, "pool_size * num_kv_heads must be < 2^31 for extend");
   const PlanHeader h = plan->hdr();
   const int e = launch_extend(desc, &h, k_pool, v_pool, q, o, lse, workspace, stream);
   return e ? cuda_fail(e, "extend launch") : RX_OK;
