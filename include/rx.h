@@ -147,6 +147,30 @@ rx_status rx_decode_attn(const rx_plan* plan, const rx_kv_desc* desc, const void
                          const void* v_pool, const void* q, void* o, float* lse,
                          void* workspace, size_t workspace_bytes, rx_stream_t stream);
 
+/* ---------------------------------------------------------------------------------------------
+ * rx_decode_attn_noalloc -- rx_decode_attn for callers that cannot allocate device memory.
+ * The pages have no counterpart: this is a convenience of the library, not a step of the method.
+ *
+ * Some callers have no way to allocate device memory when attention runs: a host framework that
+ * hands a custom operator only its input and output buffers, or a serving runtime that owns all
+ * device memory under a fixed budget and does not allow allocation while requests are in flight.
+ * This call needs no workspace: the plan's tables and the partial results live in a scratch array
+ * inside the library itself (RX_NOALLOC_SCRATCH_BYTES of device memory that every GPU loading the
+ * library holds until the process exits).  It allocates nothing.
+ *   plan      a decode plan (rx_decode_plan); it is copied into the scratch on every call, so no
+ *             rx_plan_upload is needed.  A plan needing more than RX_NOALLOC_SCRATCH_BYTES (see
+ *             rx_plan_workspace_size) is rejected with RX_ERR_WORKSPACE before anything runs.
+ *   others    as for rx_decode_attn (caller-owned device tensors; work enqueued on `stream`).
+ * The first call on a device sets up the scratch's device address for that device; make it before
+ * any stream capture.  All calls share the one array: calls whose work overlaps on the GPU (other
+ * streams, other host threads) race on it and must not be issued.  Device-side errors are recorded
+ * in the scratch and cleared by the next call; they cannot be read back with rx_read_status.
+ * ------------------------------------------------------------------------------------------- */
+#define RX_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+rx_status rx_decode_attn_noalloc(const rx_plan* plan, const rx_kv_desc* desc, const void* k_pool,
+                                 const void* v_pool, const void* q, void* o, float* lse,
+                                 rx_stream_t stream);
+
 /* Read (synchronously, on `stream`) and clear the device status word of a workspace that a plan
  * was uploaded to.  *status receives RX_OK or the first device-side error recorded. */
 rx_status rx_read_status(const void* workspace, int32_t* status, rx_stream_t stream);

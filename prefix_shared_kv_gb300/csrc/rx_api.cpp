@@ -140,6 +140,25 @@ rx_status check_plan_use(const rx_plan* p, int kind, const rx_kv_desc* d, const 
 
 }  // namespace
 
+rx_status rx::set_error(rx_status st, const char* msg) { return fail(st, "%s", msg); }
+
+rx_status rx::plan_for_noalloc(const rx_plan* plan, const rx_kv_desc* desc, const void* k,
+                               const void* v, const void* q, const void* o, const void* lse,
+                               const void* scratch, size_t scratch_bytes, const void** blob,
+                               size_t* blob_bytes, PlanHeader* hdr) {
+  if (plan && plan->kind == 2 && plan->ws_bytes > scratch_bytes)
+    return fail(RX_ERR_WORKSPACE,
+                "rx_decode_attn_noalloc: the plan needs %zu bytes of scratch, the library holds "
+                "%zu; use rx_decode_attn with a workspace for batches this large",
+                plan->ws_bytes, scratch_bytes);
+  rx_status st = check_plan_use(plan, 2, desc, k, v, q, o, lse, scratch, scratch_bytes);
+  if (st) return st;
+  *blob = plan->blob.data();
+  *blob_bytes = plan->blob.size();
+  *hdr = plan->hdr();
+  return RX_OK;
+}
+
 extern "C" {
 
 const char* rx_status_string(int s) {

@@ -22,7 +22,7 @@ RX_OK, RX_ERR_INVALID, RX_ERR_RANGE, RX_ERR_UNSUPPORTED, RX_ERR_CUDA, RX_ERR_TIM
 EXPORTED = [
     "rx_status_string", "rx_last_error", "rx_store_kv", "rx_plan_create", "rx_plan_destroy",
     "rx_plan_workspace_size", "rx_plan_upload", "rx_extend_plan", "rx_extend_attn",
-    "rx_decode_plan", "rx_decode_attn", "rx_read_status", "rx_radix_create", "rx_radix_destroy",
+    "rx_decode_plan", "rx_decode_attn", "rx_decode_attn_noalloc", "rx_read_status", "rx_radix_create", "rx_radix_destroy",
     "rx_radix_insert", "rx_radix_match", "rx_radix_stats", "rx_saved_tokens", "rx_token_saving",
     "rx_compute_reduction",
 ]
@@ -71,6 +71,7 @@ def lib():
                                      C.c_int32, _I32P]),
         "rx_decode_attn": (C.c_int, [_P, C.POINTER(KVDesc), _P, _P, _P, _P, _P, _P, C.c_size_t,
                                      _P]),
+        "rx_decode_attn_noalloc": (C.c_int, [_P, C.POINTER(KVDesc), _P, _P, _P, _P, _P, _P]),
         "rx_read_status": (C.c_int, [_P, _I32P, _P]),
         "rx_radix_create": (C.c_int, [C.POINTER(_P)]),
         "rx_radix_destroy": (None, [_P]),
@@ -213,6 +214,15 @@ def decode_attn(plan: Plan, desc: KVDesc, k_pool, v_pool, q, o, lse, workspace, 
     _check(lib().rx_decode_attn(plan.handle, C.byref(desc), _ptr(k_pool), _ptr(v_pool), _ptr(q),
                                 _ptr(o), _ptr(lse), _ptr(workspace), _nbytes(workspace),
                                 _stream(stream)))
+
+
+def decode_attn_noalloc(plan: Plan, desc: KVDesc, k_pool, v_pool, q, o, lse, stream=None):
+    """rx_decode_attn_noalloc: decode without a workspace (the library's own scratch is used)."""
+    _check(lib().rx_decode_attn_noalloc(plan.handle, C.byref(desc), _ptr(k_pool), _ptr(v_pool),
+                                        _ptr(q), _ptr(o), _ptr(lse), _stream(stream)))
+
+
+NOALLOC_SCRATCH_BYTES = 64 << 20
 
 
 def read_status(workspace, stream=None) -> int:
