@@ -9,20 +9,22 @@
 // keys (visible to that member's rows only, causal on its new tokens).  One online softmax runs
 // across all segments, so no partial results leave the CTA.
 //
-// Blackwell tile loop (one CTA per work item, 256 threads, warp-specialised, 64 keys per step):
-//   warp 4     K producer, warp 5 V producer: gather the keys' 256-byte rows by slot with TMA
-//              (cp.async.bulk.tensor tile::gather4: four pool rows per instruction, 128-byte
-//              swizzle applied by the copy engine) into 6-stage rings laid out as UMMA tiles;
-//              slot indices are fetched two steps ahead; a stage completes on its mbarrier's
-//              transaction count.
-//   warp 6     MMA issuer (one thread): S = Q K^T with tcgen05.mma (both operands K-major in
-//              shared memory, fp32 accumulator in TMEM, double-buffered), then O += P V with P
-//              read from TMEM and V as an MN-major shared-memory operand.
-//   warps 0-3  softmax: thread r owns query row r (TMEM lane r) and copies it into the Q tile
-//              first; per step: tcgen05.ld of its S row, masks,
-//              online max / sum in base 2 (the running max is only moved -- and O in TMEM
-//              rescaled -- when it grows by more than 2^8), P = exp2(.) packed to bf16 and written
-//              to its own TMEM columns with tcgen05.st for the PV MMA; finally O / l and the LSE.
+// Blackwell tile loop (one CTA per work item = two 128-row tiles A and B of one KV head, 416
+// threads, warp-specialised, 64 keys per step; every K/V step feeds both tiles, i.e. 256 rows):
+//   warps 8-9  K producers (even / odd steps), warps 10-11 V producers: gather the keys'
+//              256-byte rows by slot with TMA (cp.async.bulk.tensor tile::gather4: four pool rows
+//              per instruction, 128-byte swizzle applied by the copy engine) into 5-stage rings
+//              laid out as UMMA tiles; slot indices are fetched one step of their own ahead; a
+//              stage completes on its mbarrier's transaction count.
+//   warp 12    MMA issuer (one thread), alternating the tiles so one tile's softmax overlaps the
+//              other tile's MMAs: S_X = Q_X K^T with tcgen05.mma (K-major operands in shared
+//              memory, fp32 accumulator in TMEM), O_X += P_X V with P_X read from TMEM and V as an
+//              MN-major shared-memory operand.
+//   warps 0-3 (tile A), 4-7 (tile B)  softmax: thread r of a group owns row r of its tile (TMEM
+//              lane r) and copies it into the tile's Q buffer first; per step: tcgen05.ld of its
+//              S row, masks, online max / sum in base 2 (the running max is only moved -- and O in
+//              TMEM rescaled -- when it grows by more than 2^8), P = exp2(.) packed to bf16 and
+//              written to TMEM with tcgen05.st for the PV MMA; finally O / l and the LSE.
 // Every mbarrier wait is bounded (globaltimer); a timeout records RX_ERR_TIMEOUT in the
 // workspace status word and every role leaves its loop.
 #include <cuda.h>
@@ -55,26 +57,28 @@ struct ExtParams {
   int32_t oob_row;  // a row index past the end of the pool's [pool_size * Hkv, 128] view
 };
 
-constexpr int kThreads = 256;           // warps 0-3 softmax, 4 K producer, 5 V producer, 6 MMA
+constexpr int kThreads = 416;           // 0-7 softmax (A, B), 8-9 K, 10-11 V producers, 12 MMA
 constexpr int kN = 64;                  // keys per step
-constexpr int kStages = 6;              // K ring and V ring depth
-constexpr int kQHalf = 128 * 128;       // one 64-column half of the 128-row query tile: 16 KiB
+constexpr int kStages = 5;              // K ring and V ring depth
+constexpr int kQHalf = 128 * 128;       // one 64-column half of a 128-row query tile: 16 KiB
+constexpr int kQTile = 2 * kQHalf;      // 32 KiB
 constexpr int kKVHalf = kN * 128;       // one 64-column half of a 64-key K or V tile: 8 KiB
 constexpr int kKVTile = 2 * kKVHalf;    // 16 KiB
-constexpr int kOffQ = 0;
-constexpr int kOffK = 2 * kQHalf;
+constexpr int kOffQ = 0;                // tile A, then tile B
+constexpr int kOffK = 2 * kQTile;
 constexpr int kOffV = kOffK + kStages * kKVTile;
 constexpr int kOffBar = kOffV + kStages * kKVTile;
 // Barriers (each waiter is at most one phase behind the barrier it tests):
-//   K_FULL[k] / V_FULL[k]   step in ring stage k landed (producer warp, 32 arrivals)
-//   K_FREE[k]  S(t) = Q K(t)^T complete, K stage free           (commit after S(t))
-//   S_FULL[b]  S(t) readable by the softmax, b = t & 1          (commit after S(t))
-//   V_FREE[k]  O += P(u) V(u) complete, V stage free             (commit after PV(u))
-//   PV_DONE    PV(u) complete for u < last, O stable for a rescale (commit after PV(u))
-//   PV_LAST    the last PV complete, O final for the epilogue
-//   P_FULL[b]  P(t) in TMEM (128 softmax threads)
-// (a tcgen05.commit tracks every MMA the thread issued before it, so several commits may follow
-// one batch of MMAs)
+//   K_FULL[k] / V_FULL[k]   step landed in ring stage k (expect_tx by the producer + TMA bytes)
+//   K_FREE[k]  S_B(t) complete (both tiles have read K(t)), K stage free   (commit after S_B(t))
+//   V_FREE[k]  PV_B(t) complete (both tiles have read V(t)), V stage free  (commit after PV_B(t))
+//   S_FULL[x]  S_x(t) complete, readable by tile x's softmax              (commit after S_x(t))
+//   P_FULL[x]  P_x(t) in TMEM (tile x's 128 softmax threads)
+//   PV_LAST[x] the last PV of tile x complete: O_x final for the epilogue
+//   Q_FULL     both query tiles in shared memory (256 softmax threads)
+// S_x(t + 1) is issued after PV_x(t) and a tcgen05.commit tracks every MMA issued before it, so
+// when S_FULL[x] fires for step t + 1, PV_x(t) has completed: O_x is stable during the softmax of
+// a step and can be rescaled there without another wait.
 enum {
   B_K_FULL = 0,
   B_K_FREE = B_K_FULL + kStages,
@@ -82,18 +86,19 @@ enum {
   B_V_FREE = B_V_FULL + kStages,
   B_S_FULL = B_V_FREE + kStages,
   B_P_FULL = B_S_FULL + 2,
-  B_Q_FULL = B_P_FULL + 2,
-  B_PV_DONE,
-  B_PV_LAST,
+  B_PV_LAST = B_P_FULL + 2,
+  B_Q_FULL = B_PV_LAST + 2,
   B_COUNT
 };
 constexpr int kOffTmem = kOffBar + B_COUNT * 8;
 constexpr int kOffAbort = kOffTmem + 8;
 constexpr size_t kSmem = 1024 + kOffAbort + 16;
-// TMEM columns: S0 [0,64), S1 [64,128), O [128,256), P0 [256,288), P1 [288,320)
+// TMEM columns: S_A [0,64), S_B [64,128), O_A [128,256), O_B [256,384), P_A [384,416),
+// P_B [416,448)
 constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColS = 0;
 constexpr uint32_t kColO = 128;
-constexpr uint32_t kColP = 256;
+constexpr uint32_t kColP = 384;
 constexpr uint64_t kWaitNs = 2000000000ull;
 
 static_assert(kSmem <= 227 * 1024, "shared memory budget");
@@ -150,33 +155,35 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t mbar, uint32_t bytes) {
                : "memory");
 }
 
-// Producer warp of one operand (K or V).  The pool is viewed by the tensor map as rows of 128
-// bf16 (row = slot * Hkv + head).  Lane j fetches the table entries of keys j and j + 32 two
-// steps ahead; per step lane j then gathers keys 4 (j % 16) .. 4 (j % 16) + 3, half j / 16 of
-// their 256-byte rows, with one tile::gather4 (32 gathers = the 64 keys' K or V).  Keys past the
-// segment (or flagged entries) read a row past the end of the map, which the TMA fills with zeros.
-// The step loop is unrolled by three so the prefetched entries rotate through registers by
-// position: copying a register whose load is still in flight would wait for the load.
+// Producer warp of one operand (K or V) for every other step (t0, t0 + 2, ...).  The pool is
+// viewed by the tensor map as rows of 128 bf16 (row = slot * Hkv + head).  Lane j fetches the
+// table entries of keys j and j + 32 of its next step while issuing the current one; per step
+// lane j gathers keys 4 (j % 16) .. 4 (j % 16) + 3, half j / 16 of their 256-byte rows, with one
+// tile::gather4 (32 gathers = the 64 keys' K or V).  Keys past the segment (or flagged entries)
+// read a row past the end of the map, which the TMA fills with zeros.  The loop is unrolled by
+// two so the prefetched entries alternate between two register pairs: copying a register whose
+// load is still in flight would wait for the load.
 struct SlotPair {
   int lo, hi;  // entries of keys lane and lane + 32
 };
 
 __device__ __forceinline__ void producer(const ExtParams& p, const ExtItem& it,
-                                         const ExtSeg* segs, int ntiles, uint32_t base,
+                                         const ExtSeg* segs, int ntiles, int t0, uint32_t base,
                                          const CUtensorMap* map, uint32_t ring, int b_full,
                                          int b_free, volatile int* abort) {
   const int lane = threadIdx.x & 31;
   const int g = lane & 15, h = lane >> 4;
   const uint32_t bar = base + kOffBar;
   TileIter ahead{0, segs[0].k_begin};
-  auto fetch_next = [&](SlotPair& sp) {  // entries of the step `ahead` points at, then advance
+  for (int i = 0; i < t0; ++i) tile_next(ahead, segs, it.n_seg);
+  auto fetch_next = [&](SlotPair& sp) {  // entries of the step `ahead` points at, then skip two
     sp.lo = fetch_slot(p, segs[ahead.seg], ahead.k0, lane);
     sp.hi = fetch_slot(p, segs[ahead.seg], ahead.k0, 32 + lane);
     tile_next(ahead, segs, it.n_seg);
+    tile_next(ahead, segs, it.n_seg);
   };
-  SlotPair s0{-1, -1}, s1{-1, -1}, s2{-1, -1};
-  if (ntiles > 0) fetch_next(s0);
-  if (ntiles > 1) fetch_next(s1);
+  SlotPair s0{-1, -1}, s1{-1, -1};
+  if (t0 < ntiles) fetch_next(s0);
   bool ok = true;
   // one step: prefetch step t + 2 into `later`, wait for the stage, gather step t from `cur`
   auto step = [&](int t, const SlotPair& cur, SlotPair& later) {
@@ -206,10 +213,9 @@ __device__ __forceinline__ void producer(const ExtParams& p, const ExtItem& it,
     tma_gather4(ring + st * kKVTile + h * kKVHalf + g * 512, map, 64 * h, r[0], r[1], r[2], r[3],
                 bar + 8 * (b_full + st));
   };
-  for (int t = 0; ok && t < ntiles; t += 3) {
-    step(t, s0, s2);
-    step(t + 1, s1, s0);
-    step(t + 2, s2, s1);
+  for (int t = t0; ok && t < ntiles; t += 4) {
+    step(t, s0, s1);
+    step(t + 2, s1, s0);
   }
 }
 
@@ -219,49 +225,64 @@ __device__ __forceinline__ void mma_issuer(const ExtParams& p, int ntiles, uint3
   constexpr uint32_t idO = tc::idesc_bf16(128, 128, false, true);
   const uint32_t bar = base + kOffBar;
   uint32_t last_bar = 0, last_parity = 0;  // the most recent commit, drained before exit
-  auto pv = [&](int u) -> bool {
-    const int vs = u % kStages;
-    if (!tc::mbar_wait(bar + 8 * (B_P_FULL + (u & 1)), (u >> 1) & 1, abort, p.status, kWaitNs))
-      return false;
-    if (!tc::mbar_wait(bar + 8 * (B_V_FULL + vs), (u / kStages) & 1, abort, p.status, kWaitNs))
-      return false;
-    tc::fence_after();
-    const uint32_t vb = base + kOffV + vs * kKVTile;
-    const uint32_t pcol = tmem + kColP + (u & 1) * (kN / 2);
-#pragma unroll
-    for (int s = 0; s < kN / 16; ++s)
-      tc::mma_ts(tmem + kColO, pcol + 8 * s, tc::desc_sw128(vb + s * 2048, kKVHalf, 1024), idO,
-                 (u > 0 || s > 0) ? 1u : 0u);
-    const bool last = u == ntiles - 1;
-    tc::commit(bar + 8 * (B_V_FREE + vs));
-    tc::commit(bar + 8 * (last ? B_PV_LAST : B_PV_DONE));
-    last_bar = bar + 8 * (last ? B_PV_LAST : B_PV_DONE);
-    last_parity = last ? 0 : (u & 1);
-    return true;
+  bool ok = true;
+  auto wait = [&](int b, uint32_t parity) {
+    ok = ok && tc::mbar_wait(bar + 8 * b, parity, abort, p.status, kWaitNs);
+    return ok;
   };
-  bool ok = tc::mbar_wait(bar + 8 * B_Q_FULL, 0, abort, p.status, kWaitNs);
-  for (int t = 0; ok && t < ntiles; ++t) {
-    const int ks = t % kStages;
-    if (!tc::mbar_wait(bar + 8 * (B_K_FULL + ks), (t / kStages) & 1, abort, p.status, kWaitNs)) {
-      ok = false;
-      break;
-    }
-    tc::fence_after();
-    const uint32_t qb = base + kOffQ;
-    const uint32_t kb = base + kOffK + ks * kKVTile;
+  auto qk = [&](int x, int t) {  // S_x(t) = Q_x K(t)^T
+    const uint32_t qb = base + kOffQ + x * kQTile;
+    const uint32_t kb = base + kOffK + (t % kStages) * kKVTile;
 #pragma unroll
     for (int s = 0; s < 8; ++s) {
       const uint32_t koff = (s & 3) * 32;
-      tc::mma_ss(tmem + (t & 1) * kN, tc::desc_sw128(qb + (s >> 2) * kQHalf + koff, 16, 1024),
+      tc::mma_ss(tmem + kColS + x * kN, tc::desc_sw128(qb + (s >> 2) * kQHalf + koff, 16, 1024),
                  tc::desc_sw128(kb + (s >> 2) * kKVHalf + koff, 16, 1024), idS, s > 0 ? 1u : 0u);
     }
-    tc::commit(bar + 8 * (B_K_FREE + ks));
-    tc::commit(bar + 8 * (B_S_FULL + (t & 1)));
-    last_bar = bar + 8 * (B_S_FULL + (t & 1));
-    last_parity = (t >> 1) & 1;
-    if (t >= 1 && !pv(t - 1)) ok = false;
+    tc::commit(bar + 8 * (B_S_FULL + x));
+    last_bar = bar + 8 * (B_S_FULL + x);
+    last_parity = t & 1;
+  };
+  auto pv = [&](int x, int t) {  // O_x += P_x(t) V(t)
+    const uint32_t vb = base + kOffV + (t % kStages) * kKVTile;
+    const uint32_t pcol = tmem + kColP + x * (kN / 2);
+#pragma unroll
+    for (int s = 0; s < kN / 16; ++s)
+      tc::mma_ts(tmem + kColO + x * 128, pcol + 8 * s,
+                 tc::desc_sw128(vb + s * 2048, kKVHalf, 1024), idO, (t > 0 || s > 0) ? 1u : 0u);
+    if (t == ntiles - 1) {
+      tc::commit(bar + 8 * (B_PV_LAST + x));
+      last_bar = bar + 8 * (B_PV_LAST + x);
+      last_parity = 0;
+    }
+  };
+  if (ntiles > 0 && wait(B_Q_FULL, 0) && wait(B_K_FULL, 0)) {
+    tc::fence_after();
+    qk(0, 0);
+    qk(1, 0);
+    tc::commit(bar + 8 * B_K_FREE);
   }
-  if (ok && ntiles > 0) pv(ntiles - 1);
+  for (int t = 0; ok && t < ntiles; ++t) {
+    const int st = t % kStages, st1 = (t + 1) % kStages;
+    // tile A: its PV for step t, then its S for step t + 1
+    if (!wait(B_P_FULL + 0, t & 1) || !wait(B_V_FULL + st, (t / kStages) & 1)) break;
+    tc::fence_after();
+    pv(0, t);
+    if (t + 1 < ntiles) {
+      if (!wait(B_K_FULL + st1, ((t + 1) / kStages) & 1)) break;
+      tc::fence_after();
+      qk(0, t + 1);
+    }
+    // tile B: the same, then the stages both tiles have finished with
+    if (!wait(B_P_FULL + 1, t & 1)) break;
+    tc::fence_after();
+    pv(1, t);
+    tc::commit(bar + 8 * (B_V_FREE + st));
+    if (t + 1 < ntiles) {
+      qk(1, t + 1);
+      tc::commit(bar + 8 * (B_K_FREE + st1));
+    }
+  }
   // drain: the MMAs issued above complete before TMEM is released
   if (last_bar) tc::mbar_wait(last_bar, last_parity, abort, p.status, kWaitNs);
 }
@@ -309,26 +330,29 @@ __device__ __forceinline__ float row_exp(const uint32_t (&sr)[2][32], int n_ok, 
 __device__ __forceinline__ void softmax_rows(const ExtParams& p, const ExtItem& it,
                                              const ExtSeg* segs, int ntiles, uint32_t base,
                                              uint32_t tmem, volatile int* abort) {
-  const int r = threadIdx.x;  // query row == TMEM lane
-  const int warp = r >> 5;
-  const uint32_t lane_t = tmem + ((uint32_t)(32 * warp) << 16);
+  const int x = threadIdx.x >> 7;   // tile: 0 = A, 1 = B
+  const int r = threadIdx.x & 127;  // query row of the tile == TMEM lane
+  const int wq = (threadIdx.x >> 5) & 3;
+  const uint32_t lane_t = tmem + ((uint32_t)(32 * wq) << 16);
+  const uint32_t col_s = kColS + x * kN, col_o = kColO + x * 128, col_p = kColP + x * (kN / 2);
   const uint32_t bar = base + kOffBar;
-  const int n_rows = it.n_tok * p.gq;
+  const int n_rows = it.n_tok[x] * p.gq;
   const bool valid = r < n_rows;
   int owner = -2, kmax = 0, q_row = 0;
   if (valid) {
-    const ExtRow e = p.rows[it.row_begin + r / p.gq];
+    const ExtRow e = p.rows[it.row_begin[x] + r / p.gq];
     owner = e.owner;
     kmax = e.kmax;
     q_row = e.q_row;
   }
+  const int qh = it.kv_head * p.gq + (r % p.gq);
   {
-    // query row r -> the Q tile (16 chunks of 16 bytes), then visible to the tensor core
-    const int qh = it.kv_head * p.gq + (r % p.gq);
+    // query row r -> the tile's Q buffer (16 chunks of 16 bytes), then visible to the tensor core
     const __nv_bfloat16* src = p.q + ((int64_t)q_row * p.hq + qh) * kHeadDim;
+    const uint32_t qb = base + kOffQ + x * kQTile;
 #pragma unroll
     for (int c = 0; c < 16; ++c)
-      cp_async16(base + kOffQ + tile_off(r, c, kQHalf), valid ? src + c * 8 : p.q, valid);
+      cp_async16(qb + tile_off(r, c, kQHalf), valid ? src + c * 8 : p.q, valid);
     cp_async_commit();
     cp_async_wait<0>();
     tc::fence_proxy_async();
@@ -339,9 +363,7 @@ __device__ __forceinline__ void softmax_rows(const ExtParams& p, const ExtItem& 
   TileIter cur{0, segs[0].k_begin};
   bool ok = true;
   for (int t = 0; t < ntiles; ++t) {
-    const int b = t & 1;
-    const bool w_ok = tc::mbar_wait(bar + 8 * (B_S_FULL + b), (t >> 1) & 1, abort, p.status,
-                                    kWaitNs);
+    const bool w_ok = tc::mbar_wait(bar + 8 * (B_S_FULL + x), t & 1, abort, p.status, kWaitNs);
     if (__any_sync(0xffffffffu, !w_ok)) {  // the warp leaves together
       ok = false;
       break;
@@ -352,8 +374,8 @@ __device__ __forceinline__ void softmax_rows(const ExtParams& p, const ExtItem& 
     const int lim = vis ? min(kmax, sg.k_end) : 0;  // keys at positions >= lim are masked
     const int n_ok = max(0, min(kN, lim - cur.k0));
     uint32_t sr[2][32];
-    tc::ld32(lane_t + b * kN, sr[0]);
-    tc::ld32(lane_t + b * kN + 32, sr[1]);
+    tc::ld32(lane_t + col_s, sr[0]);
+    tc::ld32(lane_t + col_s + 32, sr[1]);
     tc::wait_ld();
     // the unmasked path only when the whole warp takes it: the tcgen05.ld/st around these
     // loops are warp-collective and must not be reached from diverged paths
@@ -362,23 +384,17 @@ __device__ __forceinline__ void softmax_rows(const ExtParams& p, const ExtItem& 
     const float m_new = n_ok > 0 ? fmaxf(m_used, mx * sl2) : m_used;
     const bool need = m_new > m_used + 8.f;
     if (__any_sync(0xffffffffu, need)) {
+      // O_x is stable here: PV_x(t-1) completed before S_x(t) (see the barrier notes)
       const float alpha = need ? fast_exp2(m_used - m_new) : 1.f;  // exp2(-inf) = 0
       if (t > 0) {
-        const bool w2 = tc::mbar_wait(bar + 8 * B_PV_DONE, (t - 1) & 1, abort, p.status,
-                                      kWaitNs);
-        if (__any_sync(0xffffffffu, !w2)) {
-          ok = false;
-          break;
-        }
-        tc::fence_after();
 #pragma unroll 1
         for (int q4 = 0; q4 < 4; ++q4) {
           uint32_t ov[32];
-          tc::ld32(lane_t + kColO + 32 * q4, ov);
+          tc::ld32(lane_t + col_o + 32 * q4, ov);
           tc::wait_ld();
 #pragma unroll
           for (int j = 0; j < 32; ++j) ov[j] = __float_as_uint(__uint_as_float(ov[j]) * alpha);
-          tc::st32(lane_t + kColO + 32 * q4, ov);
+          tc::st32(lane_t + col_o + 32 * q4, ov);
         }
         tc::wait_st();
       }
@@ -389,23 +405,22 @@ __device__ __forceinline__ void softmax_rows(const ExtParams& p, const ExtItem& 
     const float ps = full ? row_exp<false>(sr, n_ok, sl2, m_used, pk)
                           : row_exp<true>(sr, n_ok, sl2, m_used, pk);
     l += ps;
-    tc::st32(lane_t + kColP + b * (kN / 2), pk);
+    tc::st32(lane_t + col_p, pk);
     tc::wait_st();
     tc::fence_before();
-    tc::mbar_arrive(bar + 8 * (B_P_FULL + b));
+    tc::mbar_arrive(bar + 8 * (B_P_FULL + x));
     tile_next(cur, segs, it.n_seg);
   }
   if (!ok || ntiles == 0) return;
-  const bool w_ok = tc::mbar_wait(bar + 8 * B_PV_LAST, 0, abort, p.status, kWaitNs);
+  const bool w_ok = tc::mbar_wait(bar + 8 * (B_PV_LAST + x), 0, abort, p.status, kWaitNs);
   if (__any_sync(0xffffffffu, !w_ok)) return;
   tc::fence_after();
   const float inv = l > 0.f ? 1.f / l : 0.f;
-  const int qh = it.kv_head * p.gq + (r % p.gq);
   __nv_bfloat16* dst = p.o + ((int64_t)q_row * p.hq + qh) * kHeadDim;
 #pragma unroll 1
   for (int q4 = 0; q4 < 4; ++q4) {
     uint32_t ov[32];
-    tc::ld32(lane_t + kColO + 32 * q4, ov);
+    tc::ld32(lane_t + col_o + 32 * q4, ov);
     tc::wait_ld();
     if (valid) {
       uint32_t w[16];
@@ -423,9 +438,9 @@ __device__ __forceinline__ void softmax_rows(const ExtParams& p, const ExtItem& 
         l > 0.f ? (m_used + __log2f(l)) * 0.69314718055994530942f : -CUDART_INF_F;
 }
 
-__global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(ExtParams p,
-                                                                const __grid_constant__ CUtensorMap k_map,
-                                                                const __grid_constant__ CUtensorMap v_map) {
+__global__ void __launch_bounds__(kThreads, 1)
+    extend_tc_kernel(ExtParams p, const __grid_constant__ CUtensorMap k_map,
+                     const __grid_constant__ CUtensorMap v_map) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023) & ~1023u;
@@ -442,17 +457,16 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(ExtParams p,
       tc::mbar_init(bar + 8 * (B_V_FULL + i), 1);
       tc::mbar_init(bar + 8 * (B_V_FREE + i), 1);
     }
-    tc::mbar_init(bar + 8 * (B_S_FULL + 0), 1);
-    tc::mbar_init(bar + 8 * (B_S_FULL + 1), 1);
-    tc::mbar_init(bar + 8 * (B_P_FULL + 0), 128);
-    tc::mbar_init(bar + 8 * (B_P_FULL + 1), 128);
-    tc::mbar_init(bar + 8 * B_Q_FULL, 128);
-    tc::mbar_init(bar + 8 * B_PV_DONE, 1);
-    tc::mbar_init(bar + 8 * B_PV_LAST, 1);
+    for (int x = 0; x < 2; ++x) {
+      tc::mbar_init(bar + 8 * (B_S_FULL + x), 1);
+      tc::mbar_init(bar + 8 * (B_P_FULL + x), 128);
+      tc::mbar_init(bar + 8 * (B_PV_LAST + x), 1);
+    }
+    tc::mbar_init(bar + 8 * B_Q_FULL, 256);
     *abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (warp == 6) tc::alloc(base + kOffTmem, kTmemCols);
+  if (warp == 12) tc::alloc(base + kOffTmem, kTmemCols);
   tc::fence_before();
   __syncthreads();
   tc::fence_after();
@@ -460,19 +474,20 @@ __global__ void __launch_bounds__(kThreads, 1) extend_tc_kernel(ExtParams p,
   int ntiles = 0;
   for (int s = 0; s < it.n_seg; ++s) ntiles += (segs[s].k_end - segs[s].k_begin + kN - 1) / kN;
 
-  if (warp < 4) {
+  if (warp < 8) {
     softmax_rows(p, it, segs, ntiles, base, tmem, abort);
-  } else if (warp == 6) {
+  } else if (warp < 10) {
+    producer(p, it, segs, ntiles, warp - 8, base, &k_map, base + kOffK, B_K_FULL, B_K_FREE, abort);
+  } else if (warp < 12) {
+    producer(p, it, segs, ntiles, warp - 10, base, &v_map, base + kOffV, B_V_FULL, B_V_FREE,
+             abort);
+  } else {
     if ((threadIdx.x & 31) == 0) mma_issuer(p, ntiles, base, tmem, abort);
     __syncwarp();
-  } else if (warp == 4) {
-    producer(p, it, segs, ntiles, base, &k_map, base + kOffK, B_K_FULL, B_K_FREE, abort);
-  } else if (warp == 5) {
-    producer(p, it, segs, ntiles, base, &v_map, base + kOffV, B_V_FULL, B_V_FREE, abort);
   }
   tc::fence_before();
   __syncthreads();
-  if (warp == 6) {
+  if (warp == 12) {
     tc::fence_after();
     tc::dealloc(tmem, kTmemCols);
   }

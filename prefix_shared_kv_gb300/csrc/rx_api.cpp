@@ -440,7 +440,8 @@ rx_status rx_extend_plan(rx_plan* plan, const rx_kv_desc* desc, int32_t batch,
   std::vector<ExtRow> rows;
   std::vector<ExtSeg> segs;
   struct Tile {
-    int row_begin, n_tok, seg_begin, n_seg;
+    int row_begin, n_tok;
+    std::vector<ExtSeg> segs;  // shared prefix (owner -1) first, then one per member present
     double cost;
   };
   // A unit is a group (all its tiles read the same prefix KV) or a lone request.
@@ -459,9 +460,9 @@ rx_status rx_extend_plan(rx_plan* plan, const rx_kv_desc* desc, int32_t batch,
     const int n = (int)rows.size() - first_row;
     for (int t0 = 0; t0 < n; t0 += tile_tok) {
       const int nt = std::min(tile_tok, n - t0);
-      Tile tl{first_row + t0, nt, (int)segs.size(), 0, 0.0};
+      Tile tl{first_row + t0, nt, {}, 0.0};
       if (gp > 0) {
-        segs.push_back({req_idx[reqs[0]], 0, gp, -1});
+        tl.segs.push_back({req_idx[reqs[0]], 0, gp, -1});
         tl.cost += (double)gp;
       }
       int i = 0;
@@ -471,14 +472,13 @@ rx_status rx_extend_plan(rx_plan* plan, const rx_kv_desc* desc, int32_t batch,
         while (j + 1 < nt && rows[first_row + t0 + j + 1].owner == owner) ++j;
         const int kend = rows[first_row + t0 + j].kmax;  // last row's causal limit
         if (kend > gp) {
-          segs.push_back({req_idx[owner], gp, kend, owner});
+          tl.segs.push_back({req_idx[owner], gp, kend, owner});
           tl.cost += (double)(kend - gp);
         }
         i = j + 1;
       }
-      tl.n_seg = (int)segs.size() - tl.seg_begin;
       un.cost += tl.cost;
-      un.tiles.push_back(tl);
+      un.tiles.push_back(std::move(tl));
     }
     std::stable_sort(un.tiles.begin(), un.tiles.end(),
                      [](const Tile& a, const Tile& b) { return a.cost > b.cost; });
@@ -499,8 +499,38 @@ rx_status rx_extend_plan(rx_plan* plan, const rx_kv_desc* desc, int32_t batch,
   for (int b = 0; b < batch; ++b)
     if (grp[b] < 0 && extend_len[b] > 0) emit_unit(std::vector<int>{b}, 0);
 
+  // Pair consecutive tiles of a unit (similar cost after the sort) into one item; the pair walks
+  // the union of the two segment lists (same owner: the longer range).  An odd last tile is
+  // paired with an empty one.
+  struct Pair {
+    int a, b;  // tile indices, b = -1 for none
+    int seg_begin, n_seg;
+  };
+  std::vector<std::vector<Pair>> pairs(units.size());
+  for (size_t k = 0; k < units.size(); ++k) {
+    const auto& tiles = units[k].tiles;
+    for (size_t i = 0; i < tiles.size(); i += 2) {
+      Pair pr{(int)i, i + 1 < tiles.size() ? (int)i + 1 : -1, (int)segs.size(), 0};
+      std::vector<ExtSeg> u = tiles[i].segs;
+      if (pr.b >= 0)
+        for (const ExtSeg& sg : tiles[pr.b].segs) {
+          bool merged = false;
+          for (ExtSeg& x : u)
+            if (x.owner == sg.owner && x.kv_row == sg.kv_row && x.k_begin == sg.k_begin) {
+              x.k_end = std::max(x.k_end, sg.k_end);
+              merged = true;
+              break;
+            }
+          if (!merged) u.push_back(sg);
+        }
+      segs.insert(segs.end(), u.begin(), u.end());
+      pr.n_seg = (int)u.size();
+      pairs[k].push_back(pr);
+    }
+  }
+
   // Launch order: largest unit first (longest-processing-time first across units); inside a
-  // unit, KV head outer and tiles inner, so the tiles that read the same prefix K/V of one head
+  // unit, KV head outer and pairs inner, so the tiles that read the same prefix K/V of one head
   // run in the same wave and hit in L2.
   std::vector<size_t> order(units.size());
   std::iota(order.begin(), order.end(), 0);
@@ -509,8 +539,19 @@ rx_status rx_extend_plan(rx_plan* plan, const rx_kv_desc* desc, int32_t batch,
   std::vector<ExtItem> items;
   for (size_t k : order)
     for (int h = 0; h < hkv; ++h)
-      for (const Tile& t : units[k].tiles)
-        items.push_back({t.row_begin, t.n_tok, t.seg_begin, t.n_seg, h, {0, 0, 0}});
+      for (const Pair& pr : pairs[k]) {
+        const Tile& ta = units[k].tiles[pr.a];
+        ExtItem it;
+        it.row_begin[0] = ta.row_begin;
+        it.n_tok[0] = ta.n_tok;
+        it.row_begin[1] = pr.b >= 0 ? units[k].tiles[pr.b].row_begin : 0;
+        it.n_tok[1] = pr.b >= 0 ? units[k].tiles[pr.b].n_tok : 0;
+        it.seg_begin = pr.seg_begin;
+        it.n_seg = pr.n_seg;
+        it.kv_head = h;
+        it.pad = 0;
+        items.push_back(it);
+      }
   if (items.size() > (size_t)INT32_MAX) return fail(RX_ERR_RANGE, "plan too large");
 
   PlanHeader h;

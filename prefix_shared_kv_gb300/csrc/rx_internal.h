@@ -46,9 +46,10 @@ constexpr int kDecStageBytes = 2 * 128 * kHeadDim * 2;   // K + V, 128 rows each
 constexpr size_t kDecSmemBytes = (size_t)kDecStages * kDecStageBytes + kDecMaxKeysPerItem * 4;
 
 // ---------------------------------------------------------------------------------------------
-// Extend.  A work item is a tile of up to 128 query rows (new tokens x gq query heads of one KV
-// head) and a list of key segments.  Segment owner -1 is visible to every row (a shared prefix);
-// owner r is visible only to rows of request r, and only keys at positions < the row's limit.
+// Extend.  A row tile holds up to 128 query rows (new tokens x gq query heads of one KV head); a
+// work item pairs two row tiles with one list of key segments.  Segment owner -1 is visible to
+// every row (a shared prefix); owner r is visible only to rows of request r, and only keys at
+// positions < the row's limit.
 // ---------------------------------------------------------------------------------------------
 struct ExtRow {         // one new token
   int32_t q_row;        // row in q / o / lse
@@ -64,13 +65,15 @@ struct ExtSeg {
   int32_t owner;        // -1 = all rows of the item
 };
 
+// Two row tiles (A, B) of the same KV head that walk the same key segments: every K/V step feeds
+// 256 query rows.  Tile B may be empty (n_tok[1] == 0).
 struct ExtItem {
-  int32_t row_begin;    // into ext_rows
-  int32_t n_tok;        // tokens in the tile (rows = n_tok * gq <= 128)
-  int32_t seg_begin;    // into ext_segs
+  int32_t row_begin[2];  // into ext_rows
+  int32_t n_tok[2];      // tokens per tile (rows = n_tok * gq <= 128)
+  int32_t seg_begin;     // into ext_segs: the union of both tiles' segments
   int32_t n_seg;
   int32_t kv_head;
-  int32_t pad[3];
+  int32_t pad;
 };
 
 // Workspace layout written by rx_plan_upload: a 256-byte header, then the tables, then (decode)
