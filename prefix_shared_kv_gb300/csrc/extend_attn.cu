@@ -9,17 +9,17 @@
 // keys (visible to that member's rows only, causal on its new tokens).  One online softmax runs
 // across all segments, so no partial results leave the CTA.
 //
-// Blackwell tile loop (one CTA per work item = two 128-row tiles A and B of one KV head, 416
+// Blackwell tile loop (one CTA per work item = two 128-row tiles A and B of one KV head, 448
 // threads, warp-specialised, 64 keys per step; every K/V step feeds both tiles, i.e. 256 rows):
 //   warps 8-9  K producers (even / odd steps), warps 10-11 V producers: gather the keys'
 //              256-byte rows by slot with TMA (cp.async.bulk.tensor tile::gather4: four pool rows
 //              per instruction, 128-byte swizzle applied by the copy engine) into 5-stage rings
 //              laid out as UMMA tiles; slot indices are fetched one step of their own ahead; a
 //              stage completes on its mbarrier's transaction count.
-//   warp 12    MMA issuer (one thread), alternating the tiles so one tile's softmax overlaps the
-//              other tile's MMAs: S_X = Q_X K^T with tcgen05.mma (K-major operands in shared
-//              memory, fp32 accumulator in TMEM), O_X += P_X V with P_X read from TMEM and V as an
-//              MN-major shared-memory operand.
+//   warps 12-13  MMA issuers (one thread each, one per tile): S_X = Q_X K^T with tcgen05.mma
+//              (K-major operands in shared memory, fp32 accumulator in TMEM), O_X += P_X V with
+//              P_X read from TMEM (double buffered) and V as an MN-major shared-memory operand;
+//              S_X(t+1) is issued as soon as the softmax has read S_X(t).
 //   warps 0-3 (tile A), 4-7 (tile B)  softmax: thread r of a group owns row r of its tile (TMEM
 //              lane r) and copies it into the tile's Q buffer first; per step: tcgen05.ld of its
 //              S row, masks, online max / sum in base 2 (the running max is only moved -- and O in
@@ -57,7 +57,7 @@ struct ExtParams {
   int32_t oob_row;  // a row index past the end of the pool's [pool_size * Hkv, 128] view
 };
 
-constexpr int kThreads = 416;           // 0-7 softmax (A, B), 8-9 K, 10-11 V producers, 12 MMA
+constexpr int kThreads = 448;  // 0-7 softmax (A, B), 8-9 K, 10-11 V producers, 12-13 MMA (A, B)
 constexpr int kN = 64;                  // keys per step
 constexpr int kStages = 5;              // K ring and V ring depth
 constexpr int kQHalf = 128 * 128;       // one 64-column half of a 128-row query tile: 16 KiB
@@ -70,31 +70,36 @@ constexpr int kOffV = kOffK + kStages * kKVTile;
 constexpr int kOffBar = kOffV + kStages * kKVTile;
 // Barriers (each waiter is at most one phase behind the barrier it tests):
 //   K_FULL[k] / V_FULL[k]   step landed in ring stage k (expect_tx by the producer + TMA bytes)
-//   K_FREE[k]  S_B(t) complete (both tiles have read K(t)), K stage free   (commit after S_B(t))
-//   V_FREE[k]  PV_B(t) complete (both tiles have read V(t)), V stage free  (commit after PV_B(t))
+//   K_FREE[k]  S_A(t) and S_B(t) complete, K stage free     (two arrivals: commit after each S)
+//   V_FREE[k]  PV_A(t) and PV_B(t) complete, V stage free   (two arrivals: commit after each PV)
 //   S_FULL[x]  S_x(t) complete, readable by tile x's softmax              (commit after S_x(t))
-//   P_FULL[x]  P_x(t) in TMEM (tile x's 128 softmax threads)
+//   S_READ[x]  tile x's softmax has loaded S_x(t) into registers: S_x(t+1) may be issued
+//   P_FULL[x][b]  P_x(t) in TMEM buffer b = t & 1 (tile x's 128 softmax threads)
+//   PV_DONE[x] PV_x(t) complete for t < last: O_x stable for a rescale
 //   PV_LAST[x] the last PV of tile x complete: O_x final for the epilogue
 //   Q_FULL     both query tiles in shared memory (256 softmax threads)
-// S_x(t + 1) is issued after PV_x(t) and a tcgen05.commit tracks every MMA issued before it, so
-// when S_FULL[x] fires for step t + 1, PV_x(t) has completed: O_x is stable during the softmax of
-// a step and can be rescaled there without another wait.
+// The issuer of tile x issues, per step t: S_x(t+1) (as soon as the softmax has read S_x(t)), then
+// PV_x(t).  A tcgen05.commit tracks every MMA its thread issued before it, so when S_FULL[x] fires
+// for step t+1, PV_x(t-1) has completed: a rescale of O_x in step t+1 waits only for PV_x(t), and
+// P buffer (t+1) & 1 is free again.
 enum {
   B_K_FULL = 0,
   B_K_FREE = B_K_FULL + kStages,
   B_V_FULL = B_K_FREE + kStages,
   B_V_FREE = B_V_FULL + kStages,
   B_S_FULL = B_V_FREE + kStages,
-  B_P_FULL = B_S_FULL + 2,
-  B_PV_LAST = B_P_FULL + 2,
+  B_S_READ = B_S_FULL + 2,
+  B_P_FULL = B_S_READ + 2,   // [x][b] at B_P_FULL + 2 * x + b
+  B_PV_DONE = B_P_FULL + 4,
+  B_PV_LAST = B_PV_DONE + 2,
   B_Q_FULL = B_PV_LAST + 2,
   B_COUNT
 };
 constexpr int kOffTmem = kOffBar + B_COUNT * 8;
 constexpr int kOffAbort = kOffTmem + 8;
 constexpr size_t kSmem = 1024 + kOffAbort + 16;
-// TMEM columns: S_A [0,64), S_B [64,128), O_A [128,256), O_B [256,384), P_A [384,416),
-// P_B [416,448)
+// TMEM columns: S_A [0,64), S_B [64,128), O_A [128,256), O_B [256,384), then P double buffers
+// of 32 columns: P_A0, P_A1, P_B0, P_B1 from 384
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0;
 constexpr uint32_t kColO = 128;
@@ -219,69 +224,66 @@ __device__ __forceinline__ void producer(const ExtParams& p, const ExtItem& it,
   }
 }
 
-__device__ __forceinline__ void mma_issuer(const ExtParams& p, int ntiles, uint32_t base,
+// MMA issuer of tile x (one thread): S_x(t+1) as soon as tile x's softmax has read S_x(t), then
+// PV_x(t) once P_x(t) is in TMEM.  The two tiles have an issuer each (warps 12 and 13, on
+// different SM sub-partitions), so neither tile's chain waits behind the other's; both commit to
+// the ring stages' free barriers, which therefore take two arrivals.
+__device__ __forceinline__ void mma_issuer(const ExtParams& p, int x, int ntiles, uint32_t base,
                                            uint32_t tmem, volatile int* abort) {
   constexpr uint32_t idS = tc::idesc_bf16(128, kN, false, false);
   constexpr uint32_t idO = tc::idesc_bf16(128, 128, false, true);
   const uint32_t bar = base + kOffBar;
+  // descriptors of the tile bases; an operand at byte offset o adds o >> 4 (no carry: shared
+  // memory addresses stay below 256 KiB)
+  const uint64_t qdesc = tc::desc_sw128(base + kOffQ + x * kQTile, 16, 1024);
+  const uint64_t kdesc0 = tc::desc_sw128(base + kOffK, 16, 1024);
+  const uint64_t vdesc0 = tc::desc_sw128(base + kOffV, kKVHalf, 1024);
+  const uint32_t d_s = tmem + kColS + x * kN, d_o = tmem + kColO + x * 128;
   uint32_t last_bar = 0, last_parity = 0;  // the most recent commit, drained before exit
   bool ok = true;
   auto wait = [&](int b, uint32_t parity) {
     ok = ok && tc::mbar_wait(bar + 8 * b, parity, abort, p.status, kWaitNs);
     return ok;
   };
-  auto qk = [&](int x, int t) {  // S_x(t) = Q_x K(t)^T
-    const uint32_t qb = base + kOffQ + x * kQTile;
-    const uint32_t kb = base + kOffK + (t % kStages) * kKVTile;
+  auto qk = [&](int t) {  // S_x(t) = Q_x K(t)^T; K stage free (from this tile's side)
+    const uint64_t kd = kdesc0 + (((t % kStages) * kKVTile) >> 4);
 #pragma unroll
-    for (int s = 0; s < 8; ++s) {
-      const uint32_t koff = (s & 3) * 32;
-      tc::mma_ss(tmem + kColS + x * kN, tc::desc_sw128(qb + (s >> 2) * kQHalf + koff, 16, 1024),
-                 tc::desc_sw128(kb + (s >> 2) * kKVHalf + koff, 16, 1024), idS, s > 0 ? 1u : 0u);
-    }
+    for (int s = 0; s < 8; ++s)
+      tc::mma_ss(d_s, qdesc + (((s >> 2) * kQHalf + (s & 3) * 32) >> 4),
+                 kd + (((s >> 2) * kKVHalf + (s & 3) * 32) >> 4), idS, s > 0 ? 1u : 0u);
     tc::commit(bar + 8 * (B_S_FULL + x));
+    tc::commit(bar + 8 * (B_K_FREE + t % kStages));
     last_bar = bar + 8 * (B_S_FULL + x);
     last_parity = t & 1;
   };
-  auto pv = [&](int x, int t) {  // O_x += P_x(t) V(t)
-    const uint32_t vb = base + kOffV + (t % kStages) * kKVTile;
-    const uint32_t pcol = tmem + kColP + x * (kN / 2);
+  auto pv = [&](int t) {  // O_x += P_x(t) V(t); V stage free (from this tile's side)
+    const uint64_t vd = vdesc0 + (((t % kStages) * kKVTile) >> 4);
+    const uint32_t pcol = tmem + kColP + (2 * x + (t & 1)) * (kN / 2);
 #pragma unroll
     for (int s = 0; s < kN / 16; ++s)
-      tc::mma_ts(tmem + kColO + x * 128, pcol + 8 * s,
-                 tc::desc_sw128(vb + s * 2048, kKVHalf, 1024), idO, (t > 0 || s > 0) ? 1u : 0u);
-    if (t == ntiles - 1) {
-      tc::commit(bar + 8 * (B_PV_LAST + x));
-      last_bar = bar + 8 * (B_PV_LAST + x);
-      last_parity = 0;
-    }
+      tc::mma_ts(d_o, pcol + 8 * s, vd + ((s * 2048) >> 4), idO, (t > 0 || s > 0) ? 1u : 0u);
+    tc::commit(bar + 8 * (B_V_FREE + t % kStages));
+    const int b = t == ntiles - 1 ? B_PV_LAST + x : B_PV_DONE + x;
+    tc::commit(bar + 8 * b);
+    last_bar = bar + 8 * b;
+    last_parity = t == ntiles - 1 ? 0 : (t & 1);
   };
   if (ntiles > 0 && wait(B_Q_FULL, 0) && wait(B_K_FULL, 0)) {
     tc::fence_after();
-    qk(0, 0);
-    qk(1, 0);
-    tc::commit(bar + 8 * B_K_FREE);
+    qk(0);
   }
   for (int t = 0; ok && t < ntiles; ++t) {
-    const int st = t % kStages, st1 = (t + 1) % kStages;
-    // tile A: its PV for step t, then its S for step t + 1
-    if (!wait(B_P_FULL + 0, t & 1) || !wait(B_V_FULL + st, (t / kStages) & 1)) break;
-    tc::fence_after();
-    pv(0, t);
+    if (!wait(B_S_READ + x, t & 1)) break;
     if (t + 1 < ntiles) {
-      if (!wait(B_K_FULL + st1, ((t + 1) / kStages) & 1)) break;
+      if (!wait(B_K_FULL + (t + 1) % kStages, ((t + 1) / kStages) & 1)) break;
       tc::fence_after();
-      qk(0, t + 1);
+      qk(t + 1);
     }
-    // tile B: the same, then the stages both tiles have finished with
-    if (!wait(B_P_FULL + 1, t & 1)) break;
+    if (!wait(B_P_FULL + 2 * x + (t & 1), (t >> 1) & 1) ||
+        !wait(B_V_FULL + t % kStages, (t / kStages) & 1))
+      break;
     tc::fence_after();
-    pv(1, t);
-    tc::commit(bar + 8 * (B_V_FREE + st));
-    if (t + 1 < ntiles) {
-      qk(1, t + 1);
-      tc::commit(bar + 8 * (B_K_FREE + st1));
-    }
+    pv(t);
   }
   // drain: the MMAs issued above complete before TMEM is released
   if (last_bar) tc::mbar_wait(last_bar, last_parity, abort, p.status, kWaitNs);
@@ -334,7 +336,7 @@ __device__ __forceinline__ void softmax_rows(const ExtParams& p, const ExtItem& 
   const int r = threadIdx.x & 127;  // query row of the tile == TMEM lane
   const int wq = (threadIdx.x >> 5) & 3;
   const uint32_t lane_t = tmem + ((uint32_t)(32 * wq) << 16);
-  const uint32_t col_s = kColS + x * kN, col_o = kColO + x * 128, col_p = kColP + x * (kN / 2);
+  const uint32_t col_s = kColS + x * kN, col_o = kColO + x * 128, col_p = kColP + 2 * x * (kN / 2);
   const uint32_t bar = base + kOffBar;
   const int n_rows = it.n_tok[x] * p.gq;
   const bool valid = r < n_rows;
@@ -377,6 +379,8 @@ __device__ __forceinline__ void softmax_rows(const ExtParams& p, const ExtItem& 
     tc::ld32(lane_t + col_s, sr[0]);
     tc::ld32(lane_t + col_s + 32, sr[1]);
     tc::wait_ld();
+    tc::fence_before();
+    tc::mbar_arrive(bar + 8 * (B_S_READ + x));  // S_x may now be overwritten by the next step
     // the unmasked path only when the whole warp takes it: the tcgen05.ld/st around these
     // loops are warp-collective and must not be reached from diverged paths
     const bool full = __all_sync(0xffffffffu, n_ok == kN);
@@ -384,9 +388,16 @@ __device__ __forceinline__ void softmax_rows(const ExtParams& p, const ExtItem& 
     const float m_new = n_ok > 0 ? fmaxf(m_used, mx * sl2) : m_used;
     const bool need = m_new > m_used + 8.f;
     if (__any_sync(0xffffffffu, need)) {
-      // O_x is stable here: PV_x(t-1) completed before S_x(t) (see the barrier notes)
       const float alpha = need ? fast_exp2(m_used - m_new) : 1.f;  // exp2(-inf) = 0
       if (t > 0) {
+        // O_x must hold PV_x(t-1); PV_x(t-2) has completed (see the barrier notes)
+        const bool w2 = tc::mbar_wait(bar + 8 * (B_PV_DONE + x), (t - 1) & 1, abort, p.status,
+                                      kWaitNs);
+        if (__any_sync(0xffffffffu, !w2)) {
+          ok = false;
+          break;
+        }
+        tc::fence_after();
 #pragma unroll 1
         for (int q4 = 0; q4 < 4; ++q4) {
           uint32_t ov[32];
@@ -405,10 +416,10 @@ __device__ __forceinline__ void softmax_rows(const ExtParams& p, const ExtItem& 
     const float ps = full ? row_exp<false>(sr, n_ok, sl2, m_used, pk)
                           : row_exp<true>(sr, n_ok, sl2, m_used, pk);
     l += ps;
-    tc::st32(lane_t + col_p, pk);
+    tc::st32(lane_t + col_p + (t & 1) * (kN / 2), pk);
     tc::wait_st();
     tc::fence_before();
-    tc::mbar_arrive(bar + 8 * (B_P_FULL + x));
+    tc::mbar_arrive(bar + 8 * (B_P_FULL + 2 * x + (t & 1)));
     tile_next(cur, segs, it.n_seg);
   }
   if (!ok || ntiles == 0) return;
@@ -453,13 +464,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t bar = base + kOffBar;
     for (int i = 0; i < kStages; ++i) {
       tc::mbar_init(bar + 8 * (B_K_FULL + i), 1);
-      tc::mbar_init(bar + 8 * (B_K_FREE + i), 1);
+      tc::mbar_init(bar + 8 * (B_K_FREE + i), 2);
       tc::mbar_init(bar + 8 * (B_V_FULL + i), 1);
-      tc::mbar_init(bar + 8 * (B_V_FREE + i), 1);
+      tc::mbar_init(bar + 8 * (B_V_FREE + i), 2);
     }
     for (int x = 0; x < 2; ++x) {
       tc::mbar_init(bar + 8 * (B_S_FULL + x), 1);
-      tc::mbar_init(bar + 8 * (B_P_FULL + x), 128);
+      tc::mbar_init(bar + 8 * (B_S_READ + x), 128);
+      tc::mbar_init(bar + 8 * (B_P_FULL + 2 * x), 128);
+      tc::mbar_init(bar + 8 * (B_P_FULL + 2 * x + 1), 128);
+      tc::mbar_init(bar + 8 * (B_PV_DONE + x), 1);
       tc::mbar_init(bar + 8 * (B_PV_LAST + x), 1);
     }
     tc::mbar_init(bar + 8 * B_Q_FULL, 256);
@@ -482,7 +496,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     producer(p, it, segs, ntiles, warp - 10, base, &v_map, base + kOffV, B_V_FULL, B_V_FREE,
              abort);
   } else {
-    if ((threadIdx.x & 31) == 0) mma_issuer(p, ntiles, base, tmem, abort);
+    if ((threadIdx.x & 31) == 0) mma_issuer(p, warp - 12, ntiles, base, tmem, abort);
     __syncwarp();
   }
   tc::fence_before();
