@@ -9,22 +9,27 @@
 // keys (visible to that member's rows only, causal on its new tokens).  One online softmax runs
 // across all segments, so no partial results leave the CTA.
 //
-// Blackwell tile loop (one CTA per work item = two 128-row tiles A and B of one KV head, 448
+// Blackwell tile loop (one CTA per work item = two 128-row tiles A and B of one KV head, 512
 // threads, warp-specialised, 64 keys per step; every K/V step feeds both tiles, i.e. 256 rows):
-//   warps 8-9  K producers (even / odd steps), warps 10-11 V producers: gather the keys'
+//   warps 8-10  K producers (steps t = 0, 1, 2 mod 3), warps 11-13 V producers: gather the keys'
 //              256-byte rows by slot with TMA (cp.async.bulk.tensor tile::gather4: four pool rows
 //              per instruction, 128-byte swizzle applied by the copy engine) into 5-stage rings
 //              laid out as UMMA tiles; slot indices are fetched one step of their own ahead; a
 //              stage completes on its mbarrier's transaction count.
-//   warps 12-13  MMA issuers (one thread each, one per tile): S_X = Q_X K^T with tcgen05.mma
-//              (K-major operands in shared memory, fp32 accumulator in TMEM), O_X += P_X V with
-//              P_X read from TMEM (double buffered) and V as an MN-major shared-memory operand;
-//              S_X(t+1) is issued as soon as the softmax has read S_X(t).
+//   warps 14-15  MMA issuers (one thread each, one per tile X): S_X = Q_X K^T with tcgen05.mma
+//              (K-major operands in shared memory, fp32 accumulator in TMEM) into one of two S
+//              buffers, and O_X += P_X V with P_X read from TMEM and V as an MN-major shared-
+//              memory operand.  P_X(t) is written over the upper half of the S buffer it came
+//              from, and the issuer's order per step is PV_X(t), S_X(t+2) into that buffer: the
+//              tensor pipe executes one thread's MMAs in order, so S_X(t+2) overwrites P_X(t) only
+//              after PV_X(t) has read it, and S_X(t+1) is always computed a step ahead.
 //   warps 0-3 (tile A), 4-7 (tile B)  softmax: thread r of a group owns row r of its tile (TMEM
 //              lane r) and copies it into the tile's Q buffer first; per step: tcgen05.ld of its
-//              S row, masks, online max / sum in base 2 (the running max is only moved -- and O in
-//              TMEM rescaled -- when it grows by more than 2^8), P = exp2(.) packed to bf16 and
-//              written to TMEM with tcgen05.st for the PV MMA; finally O / l and the LSE.
+//              64 scores, masks, online max / sum in base 2 (the running max is only moved -- and
+//              O in TMEM rescaled -- when it grows by more than 2^8), P = exp2(.) packed to bf16
+//              and written to TMEM with tcgen05.st for the PV MMA; finally O / l and the LSE.  The
+//              two tiles take turns for the exponentials, so each has the SM's exp units to
+//              itself while the tensor core works on the other tile.
 // Every mbarrier wait is bounded (globaltimer); a timeout records RX_ERR_TIMEOUT in the
 // workspace status word and every role leaves its loop.
 #include <cuda.h>
@@ -57,54 +62,65 @@ struct ExtParams {
   int32_t oob_row;  // a row index past the end of the pool's [pool_size * Hkv, 128] view
 };
 
-constexpr int kThreads = 448;  // 0-7 softmax (A, B), 8-9 K, 10-11 V producers, 12-13 MMA (A, B)
-constexpr int kN = 64;                  // keys per step
-constexpr int kStages = 5;              // K ring and V ring depth
-constexpr int kQHalf = 128 * 128;       // one 64-column half of a 128-row query tile: 16 KiB
-constexpr int kQTile = 2 * kQHalf;      // 32 KiB
-constexpr int kKVHalf = kN * 128;       // one 64-column half of a 64-key K or V tile: 8 KiB
-constexpr int kKVTile = 2 * kKVHalf;    // 16 KiB
-constexpr int kOffQ = 0;                // tile A, then tile B
+constexpr int kN = 64;                 // keys per step
+constexpr int kPW = 3;                 // producer warps per operand (one gather in issue each)
+constexpr int kWarpK = 8, kWarpV = kWarpK + kPW, kWarpMma = kWarpV + kPW;
+constexpr int kThreads = 32 * (kWarpMma + 2);  // softmax A, B | K producers | V producers | MMA A, B
+static_assert(kThreads == 512, "four warpgroups: the register split below assumes them");
+constexpr int kRegsLaunch = 65536 / kThreads;  // 128: what each thread is launched with
+constexpr int kRegsSoftmax = 160, kRegsOther = 96;
+static_assert(2 * kRegsSoftmax + 2 * kRegsOther == 4 * kRegsLaunch, "register split");
+constexpr int kStages = 5;             // K ring and V ring depth (64-key stages)
+// A producer warp fills every kPW-th stage of its ring and first waits for that stage to be
+// released.  That wait tests a phase parity, so it must never be two phases early: the warp's own
+// previous wait covered every step up to kPW + kStages before the current one, which rules that
+// out when the ring has at least kPW stages.
+static_assert(kStages >= kPW, "a producer could run two phases ahead");
+constexpr int kQHalf = 128 * 128;      // one 64-column half of a 128-row query tile: 16 KiB
+constexpr int kQTile = 2 * kQHalf;     // 32 KiB
+constexpr int kKVHalf = kN * 128;      // one 64-column half of a 64-key K or V tile: 8 KiB
+constexpr int kKVTile = 2 * kKVHalf;   // 16 KiB
+constexpr int kOffQ = 0;               // tile A, then tile B
 constexpr int kOffK = 2 * kQTile;
 constexpr int kOffV = kOffK + kStages * kKVTile;
 constexpr int kOffBar = kOffV + kStages * kKVTile;
 // Barriers (each waiter is at most one phase behind the barrier it tests):
 //   K_FULL[k] / V_FULL[k]   step landed in ring stage k (expect_tx by the producer + TMA bytes)
-//   K_FREE[k]  S_A(t) and S_B(t) complete, K stage free     (two arrivals: commit after each S)
-//   V_FREE[k]  PV_A(t) and PV_B(t) complete, V stage free   (two arrivals: commit after each PV)
-//   S_FULL[x]  S_x(t) complete, readable by tile x's softmax              (commit after S_x(t))
-//   S_READ[x]  tile x's softmax has loaded S_x(t) into registers: S_x(t+1) may be issued
-//   P_FULL[x][b]  P_x(t) in TMEM buffer b = t & 1 (tile x's 128 softmax threads)
-//   PV_DONE[x] PV_x(t) complete for t < last: O_x stable for a rescale
-//   PV_LAST[x] the last PV of tile x complete: O_x final for the epilogue
+//   K_FREE[k]  S_A and S_B of the step complete, K stage free  (two arrivals: a commit each)
+//   V_FREE[k]  PV_A and PV_B of the step complete, V stage free
+//   S_FULL[x][b]  S_x(t) complete in buffer b = t % 2 (phase t / 2).  The issuer commits it once
+//              per step after PV_x(t) and S_x(t+2) (S_x(t+2) only when there is such a step), so
+//              the phase of step t+1 also tells that PV_x(t-1) is complete: O_x may be rescaled.
+//   P_FULL[x][b]  P_x(t) in S buffer b = t % 2 (phase t / 2; tile x's 128 softmax threads).  One
+//              barrier per buffer: with S_x(t+1) already computed, the softmax can finish step
+//              t+1 before the issuer has taken step t, so a single barrier could run two phases
+//              ahead of the issuer; P_x(t+2) waits for S_x(t+2), which waits for P_x(t).
+//   O_DONE[x]  every MMA of tile x complete: O_x final for the epilogue, TMEM free to release
 //   Q_FULL     both query tiles in shared memory (256 softmax threads)
-// The issuer of tile x issues, per step t: S_x(t+1) (as soon as the softmax has read S_x(t)), then
-// PV_x(t).  A tcgen05.commit tracks every MMA its thread issued before it, so when S_FULL[x] fires
-// for step t+1, PV_x(t-1) has completed: a rescale of O_x in step t+1 waits only for PV_x(t), and
-// P buffer (t+1) & 1 is free again.
+//   TURN[x]    tile x's softmax may run its exponentials for the next step (128 arrivals of the
+//              other tile's softmax): A(0), B(0), A(1), B(1), ...
 enum {
   B_K_FULL = 0,
   B_K_FREE = B_K_FULL + kStages,
   B_V_FULL = B_K_FREE + kStages,
   B_V_FREE = B_V_FULL + kStages,
-  B_S_FULL = B_V_FREE + kStages,
-  B_S_READ = B_S_FULL + 2,
-  B_P_FULL = B_S_READ + 2,   // [x][b] at B_P_FULL + 2 * x + b
-  B_PV_DONE = B_P_FULL + 4,
-  B_PV_LAST = B_PV_DONE + 2,
-  B_Q_FULL = B_PV_LAST + 2,
-  B_COUNT
+  B_S_FULL = B_V_FREE + kStages,  // [x][b] at B_S_FULL + 2 * x + b
+  B_P_FULL = B_S_FULL + 4,  // [x][b] at B_P_FULL + 2 * x + b
+  B_O_DONE = B_P_FULL + 4,
+  B_Q_FULL = B_O_DONE + 2,
+  B_TURN = B_Q_FULL + 1,
+  B_COUNT = B_TURN + 2
 };
 constexpr int kOffTmem = kOffBar + B_COUNT * 8;
 constexpr int kOffAbort = kOffTmem + 8;
 constexpr size_t kSmem = 1024 + kOffAbort + 16;
-// TMEM columns: S_A [0,64), S_B [64,128), O_A [128,256), O_B [256,384), then P double buffers
-// of 32 columns: P_A0, P_A1, P_B0, P_B1 from 384
+// TMEM columns: S buffers S_A0, S_A1, S_B0, S_B1 of 64 columns from 0 (P_x(t), 64 bf16 a row, two
+// a column, over the upper half of S_x's buffer t % 2), O_A [256,384), O_B [384,512)
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0;
-constexpr uint32_t kColO = 128;
-constexpr uint32_t kColP = 384;
+constexpr uint32_t kColO = 256;
+constexpr uint32_t kPOff = 32;
 constexpr uint64_t kWaitNs = 2000000000ull;
+__host__ __device__ constexpr uint32_t col_s_of(int x, int b) { return (uint32_t)(2 * x + b) * kN; }
 
 static_assert(kSmem <= 227 * 1024, "shared memory budget");
 
@@ -160,74 +176,63 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t mbar, uint32_t bytes) {
                : "memory");
 }
 
-// Producer warp of one operand (K or V) for every other step (t0, t0 + 2, ...).  The pool is
-// viewed by the tensor map as rows of 128 bf16 (row = slot * Hkv + head).  Lane j fetches the
-// table entries of keys j and j + 32 of its next step while issuing the current one; per step
-// lane j gathers keys 4 (j % 16) .. 4 (j % 16) + 3, half j / 16 of their 256-byte rows, with one
-// tile::gather4 (32 gathers = the 64 keys' K or V).  Keys past the segment (or flagged entries)
-// read a row past the end of the map, which the TMA fills with zeros.  The loop is unrolled by
-// two so the prefetched entries alternate between two register pairs: copying a register whose
-// load is still in flight would wait for the load.
-struct SlotPair {
-  int lo, hi;  // entries of keys lane and lane + 32
+
+// Producer warp of one operand (K or V): steps t = w, w + kPW, ...  A warp has one
+// tile::gather4 in issue at a time (about a hundred cycles each), so the rate at which the rings
+// fill grows with the number of producer warps.  The pool is viewed by the tensor map as rows of
+// 128 bf16 (row = slot * Hkv + head).  Per step lane j gathers keys 4 (j % 16) .. 4 (j % 16) + 3,
+// half j / 16 of their 256-byte rows, with one tile::gather4 (32 gathers = the 64 keys' K or V);
+// it fetches those keys' table entries one step of its own ahead.  Keys past the segment (or
+// flagged entries) read a row past the end of the map, which the TMA fills with zeros.
+struct Slot4 {
+  int v[4];
 };
 
 __device__ __forceinline__ void producer(const ExtParams& p, const ExtItem& it,
-                                         const ExtSeg* segs, int ntiles, int t0, uint32_t base,
+                                         const ExtSeg* segs, int ntiles, int w, uint32_t base,
                                          const CUtensorMap* map, uint32_t ring, int b_full,
                                          int b_free, volatile int* abort) {
   const int lane = threadIdx.x & 31;
   const int g = lane & 15, h = lane >> 4;
   const uint32_t bar = base + kOffBar;
-  TileIter ahead{0, segs[0].k_begin};
-  for (int i = 0; i < t0; ++i) tile_next(ahead, segs, it.n_seg);
-  auto fetch_next = [&](SlotPair& sp) {  // entries of the step `ahead` points at, then skip two
-    sp.lo = fetch_slot(p, segs[ahead.seg], ahead.k0, lane);
-    sp.hi = fetch_slot(p, segs[ahead.seg], ahead.k0, 32 + lane);
-    tile_next(ahead, segs, it.n_seg);
-    tile_next(ahead, segs, it.n_seg);
+  TileIter at{0, segs[0].k_begin};
+  int at_step = 0;
+  auto fetch = [&](Slot4& sl, int t) {  // entries of step t (t only grows)
+    for (; at_step < t; ++at_step) tile_next(at, segs, it.n_seg);
+    const ExtSeg& sg = segs[at.seg];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) sl.v[i] = fetch_slot(p, sg, at.k0, 4 * g + i);
   };
-  SlotPair s0{-1, -1}, s1{-1, -1};
-  if (t0 < ntiles) fetch_next(s0);
-  bool ok = true;
-  // one step: prefetch step t + 2 into `later`, wait for the stage, gather step t from `cur`
-  auto step = [&](int t, const SlotPair& cur, SlotPair& later) {
-    if (!ok || t >= ntiles) return;
-    if (t + 2 < ntiles) fetch_next(later);
+  Slot4 nxt{{-1, -1, -1, -1}};
+  if (w < ntiles) fetch(nxt, w);
+  // per step: take the prefetched entries, prefetch t + kPW, wait for the stage, gather t
+  for (int t = w; t < ntiles; t += kPW) {
+    const Slot4 cur = nxt;
+    if (t + kPW < ntiles) fetch(nxt, t + kPW);
     const int st = t % kStages;
     const bool waited = t < kStages || tc::mbar_wait(bar + 8 * (b_free + st),
                                                      (t / kStages - 1) & 1, abort, p.status,
                                                      kWaitNs);
-    if (__any_sync(0xffffffffu, !waited)) {  // the warp leaves together
-      ok = false;
-      return;
-    }
-    const int v0 = check_slot(p, cur.lo), v1 = check_slot(p, cur.hi);
-    const int row0 = v0 >= 0 ? v0 * p.hkv + it.kv_head : p.oob_row;
-    const int row1 = v1 >= 0 ? v1 * p.hkv + it.kv_head : p.oob_row;
+    if (__any_sync(0xffffffffu, !waited)) break;  // the warp leaves together
     int r[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int key = 4 * g + j;  // lane-dependent: shuffle both halves, select after
-      const int x0 = __shfl_sync(0xffffffffu, row0, key & 31);
-      const int x1 = __shfl_sync(0xffffffffu, row1, key & 31);
-      r[j] = key < 32 ? x0 : x1;
+    for (int i = 0; i < 4; ++i) {
+      const int v = check_slot(p, cur.v[i]);
+      r[i] = v >= 0 ? v * p.hkv + it.kv_head : p.oob_row;
     }
     if (lane == 0) mbar_expect_tx(bar + 8 * (b_full + st), kN * kHeadDim * 2);
     __syncwarp();
     tma_gather4(ring + st * kKVTile + h * kKVHalf + g * 512, map, 64 * h, r[0], r[1], r[2], r[3],
                 bar + 8 * (b_full + st));
-  };
-  for (int t = t0; ok && t < ntiles; t += 4) {
-    step(t, s0, s1);
-    step(t + 2, s1, s0);
   }
 }
 
-// MMA issuer of tile x (one thread): S_x(t+1) as soon as tile x's softmax has read S_x(t), then
-// PV_x(t) once P_x(t) is in TMEM.  The two tiles have an issuer each (warps 12 and 13, on
-// different SM sub-partitions), so neither tile's chain waits behind the other's; both commit to
-// the ring stages' free barriers, which therefore take two arrivals.
+// MMA issuer of tile x (one thread): S_x(0) and S_x(1); then per step t, once P_x(t) is in
+// TMEM, PV_x(t) and S_x(t+2) right behind it (into the buffer P_x(t) sat in).  The two tiles have
+// an issuer each (the last two warps, on different SM sub-partitions); both commit to the ring
+// stages' free barriers, which therefore take two arrivals.  The MMAs of a step are issued back
+// to back and their commits follow them: a commit holds up the issuing thread's next barrier
+// operation until the tensor pipe has taken the MMAs before it, so every wait comes first.
 __device__ __forceinline__ void mma_issuer(const ExtParams& p, int x, int ntiles, uint32_t base,
                                            uint32_t tmem, volatile int* abort) {
   constexpr uint32_t idS = tc::idesc_bf16(128, kN, false, false);
@@ -238,95 +243,99 @@ __device__ __forceinline__ void mma_issuer(const ExtParams& p, int x, int ntiles
   const uint64_t qdesc = tc::desc_sw128(base + kOffQ + x * kQTile, 16, 1024);
   const uint64_t kdesc0 = tc::desc_sw128(base + kOffK, 16, 1024);
   const uint64_t vdesc0 = tc::desc_sw128(base + kOffV, kKVHalf, 1024);
-  const uint32_t d_s = tmem + kColS + x * kN, d_o = tmem + kColO + x * 128;
-  uint32_t last_bar = 0, last_parity = 0;  // the most recent commit, drained before exit
-  bool ok = true;
+  const uint32_t d_o = tmem + kColO + x * 128;
+  bool ok = true, issued = false;
   auto wait = [&](int b, uint32_t parity) {
     ok = ok && tc::mbar_wait(bar + 8 * b, parity, abort, p.status, kWaitNs);
     return ok;
   };
-  auto qk = [&](int t) {  // S_x(t) = Q_x K(t)^T; K stage free (from this tile's side)
+  auto qk = [&](int t) {  // S_x(t) = Q_x K(t)^T into buffer t % 2
     const uint64_t kd = kdesc0 + (((t % kStages) * kKVTile) >> 4);
+    const uint32_t d_s = tmem + col_s_of(x, t & 1);
 #pragma unroll
     for (int s = 0; s < 8; ++s)
       tc::mma_ss(d_s, qdesc + (((s >> 2) * kQHalf + (s & 3) * 32) >> 4),
                  kd + (((s >> 2) * kKVHalf + (s & 3) * 32) >> 4), idS, s > 0 ? 1u : 0u);
-    tc::commit(bar + 8 * (B_S_FULL + x));
-    tc::commit(bar + 8 * (B_K_FREE + t % kStages));
-    last_bar = bar + 8 * (B_S_FULL + x);
-    last_parity = t & 1;
+    issued = true;
   };
-  auto pv = [&](int t) {  // O_x += P_x(t) V(t); V stage free (from this tile's side)
+  auto pv = [&](int t) {  // O_x += P_x(t) V(t)
     const uint64_t vd = vdesc0 + (((t % kStages) * kKVTile) >> 4);
-    const uint32_t pcol = tmem + kColP + (2 * x + (t & 1)) * (kN / 2);
+    const uint32_t a_p = tmem + col_s_of(x, t & 1) + kPOff;
 #pragma unroll
     for (int s = 0; s < kN / 16; ++s)
-      tc::mma_ts(d_o, pcol + 8 * s, vd + ((s * 2048) >> 4), idO, (t > 0 || s > 0) ? 1u : 0u);
-    tc::commit(bar + 8 * (B_V_FREE + t % kStages));
-    const int b = t == ntiles - 1 ? B_PV_LAST + x : B_PV_DONE + x;
-    tc::commit(bar + 8 * b);
-    last_bar = bar + 8 * b;
-    last_parity = t == ntiles - 1 ? 0 : (t & 1);
+      tc::mma_ts(d_o, a_p + 8 * s, vd + ((s * 2048) >> 4), idO, (t > 0 || s > 0) ? 1u : 0u);
   };
-  if (ntiles > 0 && wait(B_Q_FULL, 0) && wait(B_K_FULL, 0)) {
-    tc::fence_after();
-    qk(0);
+  if (ntiles > 0 && wait(B_Q_FULL, 0)) {
+    for (int t = 0; t < 2 && t < ntiles; ++t) {
+      if (!wait(B_K_FULL + t, 0)) break;
+      tc::fence_after();
+      qk(t);
+      tc::commit(bar + 8 * (B_S_FULL + 2 * x + t));
+      tc::commit(bar + 8 * (B_K_FREE + t));
+    }
   }
   for (int t = 0; ok && t < ntiles; ++t) {
-    if (!wait(B_S_READ + x, t & 1)) break;
-    if (t + 1 < ntiles) {
-      if (!wait(B_K_FULL + (t + 1) % kStages, ((t + 1) / kStages) & 1)) break;
-      tc::fence_after();
-      qk(t + 1);
-    }
+    const int t2 = t + 2;
+    const bool more = t2 < ntiles;
     if (!wait(B_P_FULL + 2 * x + (t & 1), (t >> 1) & 1) ||
-        !wait(B_V_FULL + t % kStages, (t / kStages) & 1))
+        !wait(B_V_FULL + t % kStages, (t / kStages) & 1) ||
+        (more && !wait(B_K_FULL + t2 % kStages, (t2 / kStages) & 1)))
       break;
     tc::fence_after();
     pv(t);
+    if (more) qk(t2);
+    tc::commit(bar + 8 * (B_V_FREE + t % kStages));
+    tc::commit(bar + 8 * (B_S_FULL + 2 * x + (t & 1)));  // also after the last steps: see above
+    if (more) tc::commit(bar + 8 * (B_K_FREE + t2 % kStages));
   }
-  // drain: the MMAs issued above complete before TMEM is released
-  if (last_bar) tc::mbar_wait(last_bar, last_parity, abort, p.status, kWaitNs);
+  // every MMA issued above completes before O is read out and TMEM is released
+  if (issued) {
+    tc::commit(bar + 8 * (B_O_DONE + x));
+    tc::mbar_wait(bar + 8 * (B_O_DONE + x), 0, abort, p.status, kWaitNs);
+  }
 }
 
-// Row maximum of the first n_ok raw scores (all kN when !MASKED), as a tree of independent
-// maxima so the chain stays short.
-template <bool MASKED>
-__device__ __forceinline__ float row_max(const uint32_t (&sr)[2][32], int n_ok) {
+// Row maximum of the 64 raw scores (three-input maxima, eight independent chains).  Masked keys
+// hold -inf, so one code path serves every step (a smaller kernel keeps the instruction cache
+// warm for all the roles that share an SM sub-partition).
+__device__ __forceinline__ float row_max(const uint32_t (&sr)[2][32]) {
   float m[8];
 #pragma unroll
-  for (int a = 0; a < 8; ++a) m[a] = -CUDART_INF_F;
+  for (int a = 0; a < 8; ++a) m[a] = __uint_as_float(sr[0][a]);
 #pragma unroll
-  for (int q2 = 0; q2 < 2; ++q2)
+  for (int q = 0; q < 2; ++q)
 #pragma unroll
-    for (int j = 0; j < 32; ++j)
-      if (!MASKED || 32 * q2 + j < n_ok) m[j & 7] = fmaxf(m[j & 7], __uint_as_float(sr[q2][j]));
+    for (int j = 0; j < 32; j += 2)
+      if (q > 0 || j >= 8)
+        m[(j >> 1) & 7] =
+            fmax3(m[(j >> 1) & 7], __uint_as_float(sr[q][j]), __uint_as_float(sr[q][j + 1]));
 #pragma unroll
-  for (int a = 0; a < 4; ++a) m[a] = fmaxf(m[a], m[a + 4]);
-  return fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3]));
+  for (int a = 0; a < 2; ++a) m[a] = fmax3(m[a], m[a + 2], m[a + 4]);
+  return fmax3(m[0], m[1], fmaxf(m[6], m[7]));
 }
 
-// p_j = 2^(s_j * scale_log2 - m) for the first n_ok keys (0 beyond), packed to bf16 pairs in pk;
-// returns the sum of the p_j (four independent partial sums).
-template <bool MASKED>
-__device__ __forceinline__ float row_exp(const uint32_t (&sr)[2][32], int n_ok, float sl2,
-                                         float m, uint32_t (&pk)[32]) {
-  float ps[4] = {0.f, 0.f, 0.f, 0.f};
+// p_j = 2^(s_j * scale_log2 - m), packed to bf16 pairs in pk (a masked key's -inf gives 0); returns
+// the sum of the p_j.  The scale-and-shift and the sums run on packed fp32 pairs.  m is finite.
+__device__ __forceinline__ float row_exp(const uint32_t (&sr)[2][32], float sl2, float m,
+                                         uint32_t (&pk)[32]) {
+  const uint64_t k2 = f2_pack(sl2, sl2), nm2 = f2_pack(-m, -m);
+  uint64_t acc[2] = {0ull, 0ull};  // two chains of (even, odd) partial sums
 #pragma unroll
-  for (int q2 = 0; q2 < 2; ++q2)
+  for (int q = 0; q < 2; ++q)
 #pragma unroll
     for (int j = 0; j < 32; j += 2) {
-      const int c = 32 * q2 + j;
-      float p0 = fast_exp2(fmaf(__uint_as_float(sr[q2][j]), sl2, -m));
-      float p1 = fast_exp2(fmaf(__uint_as_float(sr[q2][j + 1]), sl2, -m));
-      if (MASKED) {
-        p0 = c < n_ok ? p0 : 0.f;
-        p1 = c + 1 < n_ok ? p1 : 0.f;
-      }
-      ps[(j >> 1) & 3] += p0 + p1;
-      pk[c >> 1] = pack_bf16(p0, p1);
+      float x0, x1;
+      f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[q][j]), __uint_as_float(sr[q][j + 1])), k2,
+                       nm2),
+                x0, x1);
+      const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+      acc[(j >> 1) & 1] = f2_add(acc[(j >> 1) & 1], f2_pack(p0, p1));
+      pk[16 * q + (j >> 1)] = pack_bf16(p0, p1);
     }
-  return (ps[0] + ps[1]) + (ps[2] + ps[3]);
+  float a0, a1, b0, b1;
+  f2_unpack(acc[0], a0, a1);
+  f2_unpack(acc[1], b0, b1);
+  return (a0 + a1) + (b0 + b1);
 }
 
 __device__ __forceinline__ void softmax_rows(const ExtParams& p, const ExtItem& it,
@@ -336,13 +345,14 @@ __device__ __forceinline__ void softmax_rows(const ExtParams& p, const ExtItem& 
   const int r = threadIdx.x & 127;  // query row of the tile == TMEM lane
   const int wq = (threadIdx.x >> 5) & 3;
   const uint32_t lane_t = tmem + ((uint32_t)(32 * wq) << 16);
-  const uint32_t col_s = kColS + x * kN, col_o = kColO + x * 128, col_p = kColP + 2 * x * (kN / 2);
+  const uint32_t col_o = kColO + x * 128;
   const uint32_t bar = base + kOffBar;
-  const int n_rows = it.n_tok[x] * p.gq;
+  // (selects rather than it.n_tok[x]: indexing the item with a runtime x would put it on the stack)
+  const int n_rows = (x ? it.n_tok[1] : it.n_tok[0]) * p.gq;
   const bool valid = r < n_rows;
   int owner = -2, kmax = 0, q_row = 0;
   if (valid) {
-    const ExtRow e = p.rows[it.row_begin[x] + r / p.gq];
+    const ExtRow e = p.rows[(x ? it.row_begin[1] : it.row_begin[0]) + r / p.gq];
     owner = e.owner;
     kmax = e.kmax;
     q_row = e.q_row;
@@ -364,8 +374,11 @@ __device__ __forceinline__ void softmax_rows(const ExtParams& p, const ExtItem& 
   float m_used = -CUDART_INF_F, l = 0.f;
   TileIter cur{0, segs[0].k_begin};
   bool ok = true;
+  if (x == 1 && ntiles > 0) tc::mbar_arrive(bar + 8 * B_TURN);  // tile A goes first
   for (int t = 0; t < ntiles; ++t) {
-    const bool w_ok = tc::mbar_wait(bar + 8 * (B_S_FULL + x), t & 1, abort, p.status, kWaitNs);
+    const uint32_t col_s = col_s_of(x, t & 1);
+    const bool w_ok = tc::mbar_wait(bar + 8 * (B_S_FULL + 2 * x + (t & 1)), (t >> 1) & 1, abort,
+                                    p.status, kWaitNs);
     if (__any_sync(0xffffffffu, !w_ok)) {  // the warp leaves together
       ok = false;
       break;
@@ -379,51 +392,57 @@ __device__ __forceinline__ void softmax_rows(const ExtParams& p, const ExtItem& 
     tc::ld32(lane_t + col_s, sr[0]);
     tc::ld32(lane_t + col_s + 32, sr[1]);
     tc::wait_ld();
-    tc::fence_before();
-    tc::mbar_arrive(bar + 8 * (B_S_READ + x));  // S_x may now be overwritten by the next step
-    // the unmasked path only when the whole warp takes it: the tcgen05.ld/st around these
-    // loops are warp-collective and must not be reached from diverged paths
-    const bool full = __all_sync(0xffffffffu, n_ok == kN);
-    const float mx = full ? row_max<false>(sr, n_ok) : row_max<true>(sr, n_ok);
+    const bool turn = tc::mbar_wait(bar + 8 * (B_TURN + x), t & 1, abort, p.status, kWaitNs);
+    if (__any_sync(0xffffffffu, !turn)) {
+      ok = false;
+      break;
+    }
+    if (n_ok < kN) {  // keys at n_ok and beyond are masked: -inf
+#pragma unroll
+      for (int q = 0; q < 2; ++q)
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (32 * q + j >= n_ok) sr[q][j] = 0xff800000u;
+    }
+    const float mx = row_max(sr);
     const float m_new = n_ok > 0 ? fmaxf(m_used, mx * sl2) : m_used;
     const bool need = m_new > m_used + 8.f;
-    if (__any_sync(0xffffffffu, need)) {
-      const float alpha = need ? fast_exp2(m_used - m_new) : 1.f;  // exp2(-inf) = 0
-      if (t > 0) {
-        // O_x must hold PV_x(t-1); PV_x(t-2) has completed (see the barrier notes)
-        const bool w2 = tc::mbar_wait(bar + 8 * (B_PV_DONE + x), (t - 1) & 1, abort, p.status,
-                                      kWaitNs);
-        if (__any_sync(0xffffffffu, !w2)) {
-          ok = false;
-          break;
-        }
-        tc::fence_after();
-#pragma unroll 1
-        for (int q4 = 0; q4 < 4; ++q4) {
-          uint32_t ov[32];
-          tc::ld32(lane_t + col_o + 32 * q4, ov);
-          tc::wait_ld();
-#pragma unroll
-          for (int j = 0; j < 32; ++j) ov[j] = __float_as_uint(__uint_as_float(ov[j]) * alpha);
-          tc::st32(lane_t + col_o + 32 * q4, ov);
-        }
-        tc::wait_st();
-      }
-      l *= alpha;
-      if (need) m_used = m_new;
-    }
+    const bool rescale = __any_sync(0xffffffffu, need);
+    const float alpha = need ? fast_exp2(m_used - m_new) : 1.f;  // exp2(-inf) = 0
+    if (need) m_used = m_new;
     uint32_t pk[32];
-    const float ps = full ? row_exp<false>(sr, n_ok, sl2, m_used, pk)
-                          : row_exp<true>(sr, n_ok, sl2, m_used, pk);
-    l += ps;
-    tc::st32(lane_t + col_p + (t & 1) * (kN / 2), pk);
+    // a row that has seen no visible key yet has m_used = -inf and only masked keys: any finite
+    // reference gives p = 0 for them
+    l = l * alpha + row_exp(sr, sl2, m_used == -CUDART_INF_F ? 0.f : m_used, pk);
+    if (x == 0 || t + 1 < ntiles) tc::mbar_arrive(bar + 8 * (B_TURN + 1 - x));  // other tile's turn
+    if (rescale && t > 0) {
+      // O_x must hold PV_x(t-1): the phase of step t+1 of S_FULL covers it, and PV_x(t) waits for
+      // this step's P
+      const bool w2 = tc::mbar_wait(bar + 8 * (B_S_FULL + 2 * x + ((t + 1) & 1)),
+                                    ((t + 1) >> 1) & 1, abort, p.status, kWaitNs);
+      if (__any_sync(0xffffffffu, !w2)) {
+        ok = false;
+        break;
+      }
+      tc::fence_after();
+#pragma unroll 1
+      for (int q4 = 0; q4 < 4; ++q4) {
+        uint32_t ov[32];
+        tc::ld32(lane_t + col_o + 32 * q4, ov);
+        tc::wait_ld();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) ov[j] = __float_as_uint(__uint_as_float(ov[j]) * alpha);
+        tc::st32(lane_t + col_o + 32 * q4, ov);
+      }
+    }
+    tc::st32(lane_t + col_s + kPOff, pk);
     tc::wait_st();
     tc::fence_before();
     tc::mbar_arrive(bar + 8 * (B_P_FULL + 2 * x + (t & 1)));
     tile_next(cur, segs, it.n_seg);
   }
   if (!ok || ntiles == 0) return;
-  const bool w_ok = tc::mbar_wait(bar + 8 * (B_PV_LAST + x), 0, abort, p.status, kWaitNs);
+  const bool w_ok = tc::mbar_wait(bar + 8 * (B_O_DONE + x), 0, abort, p.status, kWaitNs);
   if (__any_sync(0xffffffffu, !w_ok)) return;
   tc::fence_after();
   const float inv = l > 0.f ? 1.f / l : 0.f;
@@ -468,19 +487,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::mbar_init(bar + 8 * (B_V_FULL + i), 1);
       tc::mbar_init(bar + 8 * (B_V_FREE + i), 2);
     }
+    for (int i = 0; i < 4; ++i) {
+      tc::mbar_init(bar + 8 * (B_S_FULL + i), 1);
+      tc::mbar_init(bar + 8 * (B_P_FULL + i), 128);
+    }
     for (int x = 0; x < 2; ++x) {
-      tc::mbar_init(bar + 8 * (B_S_FULL + x), 1);
-      tc::mbar_init(bar + 8 * (B_S_READ + x), 128);
-      tc::mbar_init(bar + 8 * (B_P_FULL + 2 * x), 128);
-      tc::mbar_init(bar + 8 * (B_P_FULL + 2 * x + 1), 128);
-      tc::mbar_init(bar + 8 * (B_PV_DONE + x), 1);
-      tc::mbar_init(bar + 8 * (B_PV_LAST + x), 1);
+      tc::mbar_init(bar + 8 * (B_O_DONE + x), 1);
+      tc::mbar_init(bar + 8 * (B_TURN + x), 128);
     }
     tc::mbar_init(bar + 8 * B_Q_FULL, 256);
     *abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (warp == 12) tc::alloc(base + kOffTmem, kTmemCols);
+  if (warp == kWarpMma) tc::alloc(base + kOffTmem, kTmemCols);
   tc::fence_before();
   __syncthreads();
   tc::fence_after();
@@ -488,20 +507,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   int ntiles = 0;
   for (int s = 0; s < it.n_seg; ++s) ntiles += (segs[s].k_end - segs[s].k_begin + kN - 1) / kN;
 
-  if (warp < 8) {
+  if (warp < kWarpK) {
+    tc::regs_inc<kRegsSoftmax>();
     softmax_rows(p, it, segs, ntiles, base, tmem, abort);
-  } else if (warp < 10) {
-    producer(p, it, segs, ntiles, warp - 8, base, &k_map, base + kOffK, B_K_FULL, B_K_FREE, abort);
-  } else if (warp < 12) {
-    producer(p, it, segs, ntiles, warp - 10, base, &v_map, base + kOffV, B_V_FULL, B_V_FREE,
-             abort);
   } else {
-    if ((threadIdx.x & 31) == 0) mma_issuer(p, warp - 12, ntiles, base, tmem, abort);
-    __syncwarp();
+    tc::regs_dec<kRegsOther>();
+    if (warp < kWarpMma) {
+      const bool k = warp < kWarpV;
+      producer(p, it, segs, ntiles, warp - (k ? kWarpK : kWarpV), base, k ? &k_map : &v_map,
+               base + (k ? kOffK : kOffV), k ? B_K_FULL : B_V_FULL, k ? B_K_FREE : B_V_FREE,
+               abort);
+    } else {
+      if ((threadIdx.x & 31) == 0) mma_issuer(p, warp - kWarpMma, ntiles, base, tmem, abort);
+      __syncwarp();
+    }
   }
   tc::fence_before();
   __syncthreads();
-  if (warp == 12) {
+  if (warp == kWarpMma) {
     tc::fence_after();
     tc::dealloc(tmem, kTmemCols);
   }
@@ -539,8 +562,15 @@ int launch_extend(const rx_kv_desc* d, const PlanHeader* h, const void* k_pool,
                   void* stream) {
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(extend_tc_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
+    // The softmax warpgroups raise their register budget with what the other warpgroups give up;
+    // that only balances when every thread starts with exactly kRegsLaunch registers (with fewer,
+    // the raise would wait for registers that never come), so any other build is refused.
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, extend_tc_kernel);
+    if (e != cudaSuccess) return (int)e;
+    if (fa.numRegs != kRegsLaunch) return (int)cudaErrorInvalidConfiguration;
+    e = cudaFuncSetAttribute(extend_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kSmem);
     if (e != cudaSuccess) return (int)e;
     attr_set = true;
   }

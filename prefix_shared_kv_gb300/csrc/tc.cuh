@@ -49,6 +49,18 @@ __device__ __forceinline__ void commit(uint32_t mbar) {
       : "memory");
 }
 
+// Register budget of the calling warpgroup (all four warps execute it).  The increases of some
+// warpgroups must be covered by the decreases of others: their sum stays within the registers
+// the block was launched with.
+template <uint32_t N>
+__device__ __forceinline__ void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 __device__ __forceinline__ void fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
@@ -112,28 +124,40 @@ __device__ __forceinline__ bool mbar_try(uint32_t mbar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// As mbar_try, but a thread whose phase is not complete yet is suspended (taking no issue slots
+// from the warps that work) until the phase completes or about `hint_ns` have passed.
+__device__ __forceinline__ bool mbar_try_suspend(uint32_t mbar, uint32_t parity,
+                                                 uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+      "selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(mbar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
 __device__ __forceinline__ uint64_t globaltimer() {
   uint64_t t;
   asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
   return t;
 }
 
-// Wait for the phase of `parity` to complete.  Gives up after `limit_ns` of wall time or as soon
-// as another thread of the CTA raised *abort; on giving up it raises *abort, records
-// RX_ERR_TIMEOUT in *status (first error wins) and returns false.
+// Wait for the phase of `parity` to complete.  The waiting thread sleeps in the barrier between
+// checks instead of spinning.  Gives up after `limit_ns` of wall time or as soon as another
+// thread of the CTA raised *abort; on giving up it raises *abort, records RX_ERR_TIMEOUT in
+// *status (first error wins) and returns false.
 __device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity, volatile int* abort,
                                           int32_t* status, uint64_t limit_ns) {
   if (mbar_try(mbar, parity)) return true;
   const uint64_t t0 = globaltimer();
-  for (uint32_t i = 1;; ++i) {
-    if (mbar_try(mbar, parity)) return true;
-    if ((i & 63) == 0) {
-      if (*abort) return false;
-      if (globaltimer() - t0 > limit_ns) {
-        *abort = 1;
-        atomicCAS(status, 0, 5 /* RX_ERR_TIMEOUT */);
-        return false;
-      }
+  for (;;) {
+    if (mbar_try_suspend(mbar, parity, 20000u)) return true;
+    if (*abort) return false;
+    if (globaltimer() - t0 > limit_ns) {
+      *abort = 1;
+      atomicCAS(status, 0, 5 /* RX_ERR_TIMEOUT */);
+      return false;
     }
   }
 }
