@@ -56,11 +56,9 @@ def work_counts(wl, step=0):
         out["extend_rows"] = int(E.sum())
     if st.decode is not None:
         dc = st.decode
-        gp = np.where(dc.group_of_req >= 0,
-                      dc.group_prefix_len[np.maximum(dc.group_of_req, 0)] if len(dc.group_prefix_len) else 0,
-                      0)
-        used = set(int(g) for g in dc.group_of_req if g >= 0)
-        tokens = float(np.sum(dc.seq_len - gp)) + float(sum(dc.group_prefix_len[g] for g in used))
+        # the least the method must read: every distinct pool slot the batch attends to, once
+        slots = np.concatenate([wl.req_to_token[r, :n] for r, n in zip(dc.req_idx, dc.seq_len)])
+        tokens = float(np.unique(slots).size)
         out["decode_kv_bytes"] = tokens * hkv * d * 2 * 2
         out["decode_rows"] = int(len(dc.req_idx))
     return out
@@ -205,7 +203,7 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["rx", "reference"], default="rx")
     ap.add_argument("--workload", default="radix-mixed",
-                    choices=["radix-mixed", "extend", "decode", "gqa-decode", "tiny"])
+                    choices=sorted(W.NAMED))
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", choices=["store", "extend", "decode"], default=None,
@@ -371,7 +369,11 @@ def main():
     if has_dec:
         a = w["decode_kv_bytes"] / (part_ms["decode"] * 1e-3) / 1e9
         pdesc["decode"] = {"ms": part_ms["decode"], "GB/s": a, "frac_hbm": a / peaks["hbm_gbs"],
-                           "unique_kv_bytes": w["decode_kv_bytes"]}
+                           "unique_kv_bytes": w["decode_kv_bytes"],
+                           # what the plan's kernels read (a prefix read for two member tiles of
+                           # a group counts twice): the kernel's own bandwidth is plan bytes / ms
+                           "plan_kv_bytes": float(dw.steps[0].dec_plan.key_reads())
+                           * wl.head_dim * 2 * 2}
     if has_ext:
         dom = ("extend", "extend_attn.cu")
         roof = {"bound": "tensor", "achieved": pdesc["extend"]["TFLOP/s"],

@@ -130,6 +130,42 @@ rx_status rx_extend_attn(const rx_plan* plan, const rx_kv_desc* desc, const void
                          void* workspace, size_t workspace_bytes, rx_stream_t stream);
 
 /* ---------------------------------------------------------------------------------------------
+ * Prefix trees (SGLang explainer, "RadixAttention: Radix Tree KV cache management"; SGLang paper
+ * notes, Figure 9: tree-structured sharing).  Groups may form a forest: group_parent[g] is the
+ * group whose prefix g's prefix extends, or -1 for a root (group_parent == NULL: every group is a
+ * root).  Requirements: group_parent[g] < g (parents listed first), and
+ * group_prefix_len[parent] <= group_prefix_len[g].  A request of group g shares the first
+ * group_prefix_len[a] entries of its table row with every request of a's subtree, for each group a
+ * on the path from g to its root.  Node a's own keys are positions
+ * group_prefix_len[parent(a)] .. group_prefix_len[a]-1 (from 0 for a root).
+ *
+ * rx_extend_plan_tree: as rx_extend_plan; new rows are packed by the deepest group on a request's
+ * path that holds at least two requests with new tokens, so rows that share the most keys share
+ * tiles.  The result does not depend on the tree.
+ * rx_decode_plan_tree: as rx_decode_plan, with each node's own keys read from HBM once for all
+ * requests beneath it (one work unit per node, KV head and key chunk), each request's keys past
+ * its deepest group's prefix read once for it, and all of a request's partial softmax states
+ * combined by one log-sum-exp merge (cascade across the levels of the tree).
+ * Arrays are (host).  Errors: RX_ERR_RANGE for a parent that is not listed first or a prefix
+ * shorter than its parent's; otherwise as the one-level planners.
+ * ------------------------------------------------------------------------------------------- */
+rx_status rx_extend_plan_tree(rx_plan* plan, const rx_kv_desc* desc, int32_t batch,
+                              const int32_t* req_idx, const int32_t* prefix_len,
+                              const int32_t* extend_len, const int32_t* group_of_req,
+                              int32_t num_groups, const int32_t* group_prefix_len,
+                              const int32_t* group_parent);
+rx_status rx_decode_plan_tree(rx_plan* plan, const rx_kv_desc* desc, int32_t batch,
+                              const int32_t* req_idx, const int32_t* seq_len,
+                              const int32_t* group_of_req, int32_t num_groups,
+                              const int32_t* group_prefix_len, const int32_t* group_parent);
+
+/* Number of (key, KV head) rows of the pool the built plan's kernels read, each counted once per
+ * read (a shared prefix read for 16 members counts once; a prefix re-read for a second member
+ * tile counts twice).  With rx_kv_desc's head size this gives the plan's K+V bytes:
+ * rows * 2 * head_dim * 2.  For a tests' and a benchmark's bookkeeping; (host). */
+rx_status rx_plan_key_reads(const rx_plan* plan, int64_t* rows);
+
+/* ---------------------------------------------------------------------------------------------
  * rx_decode_plan / rx_decode_attn -- one query token per request over all of its keys, the current
  * token included (the caller stores it first).  Request b owns table row req_idx[b] and attends to
  * key positions 0..seq_len[b]-1; q/o rows are b, lse row b.

@@ -87,6 +87,7 @@ struct rx_plan {
   int kind = 0;  // 0 = empty, 1 = extend, 2 = decode
   std::vector<uint8_t> blob;  // header + tables, uploaded verbatim
   size_t ws_bytes = 0;
+  int64_t key_reads = 0;  // (key, KV head) rows of the pool the kernels read
   int32_t hq = 0, hkv = 0;
   int64_t rows = 0, stride = 0, pool = 0;
   const int32_t* table = nullptr;
@@ -200,6 +201,13 @@ rx_status rx_plan_create(rx_plan** out) {
 
 void rx_plan_destroy(rx_plan* plan) { delete plan; }
 
+rx_status rx_plan_key_reads(const rx_plan* plan, int64_t* rows) {
+  if (!plan || !rows) return fail(RX_ERR_INVALID, "NULL argument");
+  if (!plan->kind) return fail(RX_ERR_INVALID, "plan has not been built");
+  *rows = plan->key_reads;
+  return RX_OK;
+}
+
 rx_status rx_plan_workspace_size(const rx_plan* plan, size_t* bytes) {
   if (!plan || !bytes) return fail(RX_ERR_INVALID, "NULL argument");
   if (!plan->kind) return fail(RX_ERR_INVALID, "plan has not been built");
@@ -222,8 +230,24 @@ rx_status rx_plan_upload(const rx_plan* plan, void* workspace, size_t workspace_
 }
 
 // ---------------------------------------------------------------------------------------------
-// Decode planner.  Work units: (group, member tile, prefix chunk) for shared prefixes and
-// (request, own-key chunk) for the rest; each unit becomes one item per KV-head block.  Chunk
+// Validates a group forest: parents listed first, a prefix at least as long as its parent's.
+rx_status check_tree(int32_t num_groups, const int32_t* group_prefix_len,
+                     const int32_t* group_parent) {
+  for (int g = 0; g < num_groups; ++g) {
+    if (group_prefix_len[g] < 0) return fail(RX_ERR_RANGE, "group_prefix_len[%d] < 0", g);
+    if (!group_parent) continue;
+    const int pa = group_parent[g];
+    if (pa < -1 || pa >= g)
+      return fail(RX_ERR_RANGE, "group_parent[%d] = %d: parents must be listed first", g, pa);
+    if (pa >= 0 && group_prefix_len[pa] > group_prefix_len[g])
+      return fail(RX_ERR_RANGE, "group_prefix_len[%d] < its parent's", g);
+  }
+  return RX_OK;
+}
+
+// Decode planner.  Work units: (group node, member tile, chunk of the node's own keys) -- a node's
+// members are all requests of its subtree -- and (request, chunk of its keys past its deepest
+// group's prefix); each unit becomes one item per KV-head block.  Chunk
 // lengths aim at about three items' worth of bytes per SM so a longest-first launch order
 // balances; partial rows are allocated per unit over all KV heads.
 // ---------------------------------------------------------------------------------------------
@@ -231,13 +255,24 @@ rx_status rx_decode_plan(rx_plan* plan, const rx_kv_desc* desc, int32_t batch,
                          const int32_t* req_idx, const int32_t* seq_len,
                          const int32_t* group_of_req, int32_t num_groups,
                          const int32_t* group_prefix_len) {
+  return rx_decode_plan_tree(plan, desc, batch, req_idx, seq_len, group_of_req, num_groups,
+                             group_prefix_len, nullptr);
+}
+
+rx_status rx_decode_plan_tree(rx_plan* plan, const rx_kv_desc* desc, int32_t batch,
+                              const int32_t* req_idx, const int32_t* seq_len,
+                              const int32_t* group_of_req, int32_t num_groups,
+                              const int32_t* group_prefix_len, const int32_t* group_parent) {
   if (!plan) return fail(RX_ERR_INVALID, "plan is NULL");
   rx_status st = check_desc(desc, true);
   if (st) return st;
   if (batch < 0 || num_groups < 0) return fail(RX_ERR_INVALID, "negative batch or group count");
   if (batch > 0 && (!req_idx || !seq_len)) return fail(RX_ERR_INVALID, "NULL length array");
   if (num_groups > 0 && !group_prefix_len) return fail(RX_ERR_INVALID, "group_prefix_len NULL");
+  st = check_tree(num_groups, group_prefix_len, group_parent);
+  if (st) return st;
   const int hkv = desc->num_kv_heads, gq = desc->num_q_heads / hkv;
+  auto parent = [&](int g) { return group_parent ? group_parent[g] : -1; };
   std::vector<int> grp(batch, -1);
   for (int b = 0; b < batch; ++b) {
     if (req_idx[b] < 0 || req_idx[b] >= desc->req_to_token_rows)
@@ -255,9 +290,11 @@ rx_status rx_decode_plan(rx_plan* plan, const rx_kv_desc* desc, int32_t batch,
       }
     }
   }
+  // a node's members: every request of its subtree (batch order)
   std::vector<std::vector<int>> members(num_groups);
   for (int b = 0; b < batch; ++b)
-    if (grp[b] >= 0) members[grp[b]].push_back(b);
+    for (int g = grp[b]; g >= 0; g = parent(g)) members[g].push_back(b);
+  auto node_lo = [&](int g) { return parent(g) >= 0 ? group_prefix_len[parent(g)] : 0; };
 
   struct Unit {
     int kind, kv_row, k_begin, k_end, row_begin, n_tok;
@@ -275,8 +312,8 @@ rx_status rx_decode_plan(rx_plan* plan, const rx_kv_desc* desc, int32_t batch,
   const double key_bytes = 2.0 * kHeadDim * 2;
   double total = 0;
   for (int g = 0; g < num_groups; ++g)
-    if (!members[g].empty() && group_prefix_len[g] > 0)
-      total += (double)group_prefix_len[g] * hkv * key_bytes *
+    if (!members[g].empty() && group_prefix_len[g] > node_lo(g))
+      total += (double)(group_prefix_len[g] - node_lo(g)) * hkv * key_bytes *
                ((members[g].size() + max_tok - 1) / max_tok);
   for (int b = 0; b < batch; ++b)
     total += (double)(seq_len[b] - (grp[b] >= 0 ? group_prefix_len[grp[b]] : 0)) * hkv * key_bytes;
@@ -297,19 +334,20 @@ rx_status rx_decode_plan(rx_plan* plan, const rx_kv_desc* desc, int32_t batch,
   std::vector<std::pair<int, int>> ch;
 
   for (int g = 0; g < num_groups; ++g) {
-    const int gp = group_prefix_len[g];
+    const int lo = node_lo(g), hi = group_prefix_len[g];
     const auto& mem = members[g];
-    if (mem.empty() || gp == 0) continue;
+    if (mem.empty() || hi <= lo) continue;
     for (size_t t0 = 0; t0 < mem.size(); t0 += max_tok) {
       const int n_tok = (int)std::min<size_t>(max_tok, mem.size() - t0);
       const int kind = kind_of_rows(n_tok * gq);
       const int row_begin = (int)rows.size();
       for (int i = 0; i < n_tok; ++i) rows.push_back(mem[t0 + i]);
-      chunks(gp, kind, ch);
+      chunks(hi - lo, kind, ch);
       for (auto& c : ch) {
         const int64_t part = npart;
         npart += (int64_t)hkv * n_tok * gq;
-        units.push_back({kind, req_idx[mem[t0]], c.first, c.second, row_begin, n_tok, part});
+        units.push_back(
+            {kind, req_idx[mem[t0]], lo + c.first, lo + c.second, row_begin, n_tok, part});
         for (int i = 0; i < n_tok; ++i)
           refs[mem[t0 + i]].push_back({(int32_t)part, n_tok * gq, i * gq, 0});
       }
@@ -331,11 +369,13 @@ rx_status rx_decode_plan(rx_plan* plan, const rx_kv_desc* desc, int32_t batch,
   if (npart > (int64_t)INT32_MAX) return fail(RX_ERR_RANGE, "plan too large");
 
   std::vector<DecItem> items;
+  int64_t key_reads = 0;
   for (const Unit& u : units) {
     const int hb = hb_of(u.kind);
     for (int h = 0; h * hb < hkv; ++h)
       items.push_back({u.kind, h, u.kv_row, u.k_begin, u.k_end, u.row_begin, u.n_tok,
                        (int32_t)u.part});
+    key_reads += (int64_t)(u.k_end - u.k_begin) * hkv;
   }
   auto cost = [&](const DecItem& it) {
     return (double)(it.k_end - it.k_begin) * std::min(hb_of(it.kind), hkv);
@@ -378,6 +418,7 @@ rx_status rx_decode_plan(rx_plan* plan, const rx_kv_desc* desc, int32_t batch,
   put(plan->blob, h.off_merge_idx, midx);
   put(plan->blob, h.off_merge, mref);
   plan->ws_bytes = off;
+  plan->key_reads = key_reads;
   plan->kind = 2;
   remember_desc(plan, desc);
   return RX_OK;
@@ -405,6 +446,15 @@ rx_status rx_extend_plan(rx_plan* plan, const rx_kv_desc* desc, int32_t batch,
                          const int32_t* req_idx, const int32_t* prefix_len,
                          const int32_t* extend_len, const int32_t* group_of_req,
                          int32_t num_groups, const int32_t* group_prefix_len) {
+  return rx_extend_plan_tree(plan, desc, batch, req_idx, prefix_len, extend_len, group_of_req,
+                             num_groups, group_prefix_len, nullptr);
+}
+
+rx_status rx_extend_plan_tree(rx_plan* plan, const rx_kv_desc* desc, int32_t batch,
+                              const int32_t* req_idx, const int32_t* prefix_len,
+                              const int32_t* extend_len, const int32_t* group_of_req,
+                              int32_t num_groups, const int32_t* group_prefix_len,
+                              const int32_t* group_parent) {
   if (!plan) return fail(RX_ERR_INVALID, "plan is NULL");
   rx_status st = check_desc(desc, true);
   if (st) return st;
@@ -412,6 +462,8 @@ rx_status rx_extend_plan(rx_plan* plan, const rx_kv_desc* desc, int32_t batch,
   if (batch > 0 && (!req_idx || !prefix_len || !extend_len))
     return fail(RX_ERR_INVALID, "NULL length array");
   if (num_groups > 0 && !group_prefix_len) return fail(RX_ERR_INVALID, "group_prefix_len NULL");
+  st = check_tree(num_groups, group_prefix_len, group_parent);
+  if (st) return st;
   const int hkv = desc->num_kv_heads, gq = desc->num_q_heads / hkv;
   std::vector<int64_t> cu(batch + 1, 0);
   std::vector<int> grp(batch, -1);
@@ -485,9 +537,23 @@ rx_status rx_extend_plan(rx_plan* plan, const rx_kv_desc* desc, int32_t batch,
     units.push_back(std::move(un));
   };
 
-  std::vector<std::vector<int>> members(num_groups);
+  // A request's new rows go with the deepest group on its path that holds at least two requests
+  // with new tokens (rows that share the most keys share tiles); the tile's shared segment is
+  // that group's whole prefix, which is contiguous in every member's row.
+  std::vector<int> with_new(num_groups, 0);
   for (int b = 0; b < batch; ++b)
-    if (grp[b] >= 0 && extend_len[b] > 0) members[grp[b]].push_back(b);
+    if (extend_len[b] > 0)
+      for (int g = grp[b]; g >= 0; g = group_parent ? group_parent[g] : -1) ++with_new[g];
+  std::vector<std::vector<int>> members(num_groups);
+  for (int b = 0; b < batch; ++b) {
+    if (extend_len[b] <= 0 || grp[b] < 0) continue;
+    int g = grp[b];
+    while (g >= 0 && with_new[g] < 2) g = group_parent ? group_parent[g] : -1;
+    if (g >= 0)
+      members[g].push_back(b);
+    else
+      grp[b] = -1;  // alone on its path: a unit of its own below
+  }
   for (int g = 0; g < num_groups; ++g) {
     if (members[g].empty()) continue;
     if (group_prefix_len[g] > 0) {
@@ -537,6 +603,11 @@ rx_status rx_extend_plan(rx_plan* plan, const rx_kv_desc* desc, int32_t batch,
   std::stable_sort(order.begin(), order.end(),
                    [&](size_t a, size_t b) { return units[a].cost > units[b].cost; });
   std::vector<ExtItem> items;
+  int64_t key_reads = 0;
+  for (size_t k : order)
+    for (const Pair& pr : pairs[k])
+      for (int i = 0; i < pr.n_seg; ++i)
+        key_reads += (int64_t)(segs[pr.seg_begin + i].k_end - segs[pr.seg_begin + i].k_begin) * hkv;
   for (size_t k : order)
     for (int h = 0; h < hkv; ++h)
       for (const Pair& pr : pairs[k]) {
@@ -575,6 +646,7 @@ rx_status rx_extend_plan(rx_plan* plan, const rx_kv_desc* desc, int32_t batch,
   put(plan->blob, h.off_rows, rows);
   put(plan->blob, h.off_segs, segs);
   plan->ws_bytes = off;
+  plan->key_reads = key_reads;
   plan->kind = 1;
   remember_desc(plan, desc);
   return RX_OK;

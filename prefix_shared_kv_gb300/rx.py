@@ -21,8 +21,9 @@ RX_OK, RX_ERR_INVALID, RX_ERR_RANGE, RX_ERR_UNSUPPORTED, RX_ERR_CUDA, RX_ERR_TIM
 
 EXPORTED = [
     "rx_status_string", "rx_last_error", "rx_store_kv", "rx_plan_create", "rx_plan_destroy",
-    "rx_plan_workspace_size", "rx_plan_upload", "rx_extend_plan", "rx_extend_attn",
-    "rx_decode_plan", "rx_decode_attn", "rx_decode_attn_noalloc", "rx_read_status", "rx_radix_create", "rx_radix_destroy",
+    "rx_plan_workspace_size", "rx_plan_upload", "rx_plan_key_reads", "rx_extend_plan",
+    "rx_extend_plan_tree", "rx_extend_attn", "rx_decode_plan", "rx_decode_plan_tree",
+    "rx_decode_attn", "rx_decode_attn_noalloc", "rx_read_status", "rx_radix_create", "rx_radix_destroy",
     "rx_radix_insert", "rx_radix_match", "rx_radix_stats", "rx_saved_tokens", "rx_token_saving",
     "rx_compute_reduction",
 ]
@@ -63,8 +64,13 @@ def lib():
         "rx_plan_destroy": (None, [_P]),
         "rx_plan_workspace_size": (C.c_int, [_P, C.POINTER(C.c_size_t)]),
         "rx_plan_upload": (C.c_int, [_P, _P, C.c_size_t, _P]),
+        "rx_plan_key_reads": (C.c_int, [_P, _I64P]),
         "rx_extend_plan": (C.c_int, [_P, C.POINTER(KVDesc), C.c_int32, _I32P, _I32P, _I32P,
                                      _I32P, C.c_int32, _I32P]),
+        "rx_extend_plan_tree": (C.c_int, [_P, C.POINTER(KVDesc), C.c_int32, _I32P, _I32P, _I32P,
+                                          _I32P, C.c_int32, _I32P, _I32P]),
+        "rx_decode_plan_tree": (C.c_int, [_P, C.POINTER(KVDesc), C.c_int32, _I32P, _I32P, _I32P,
+                                          C.c_int32, _I32P, _I32P]),
         "rx_extend_attn": (C.c_int, [_P, C.POINTER(KVDesc), _P, _P, _P, _P, _P, _P, C.c_size_t,
                                      _P]),
         "rx_decode_plan": (C.c_int, [_P, C.POINTER(KVDesc), C.c_int32, _I32P, _I32P, _I32P,
@@ -169,6 +175,12 @@ class Plan:
         _check(lib().rx_plan_workspace_size(self._h, C.byref(n)))
         return n.value
 
+    def key_reads(self) -> int:
+        """(key, KV head) rows of the pool the plan's kernels read (rx_plan_key_reads)."""
+        n = np.zeros(1, np.int64)
+        _check(lib().rx_plan_key_reads(self._h, n.ctypes.data_as(_I64P)))
+        return int(n[0])
+
     def upload(self, workspace, nbytes: Optional[int] = None, stream=None):
         if nbytes is None:
             nbytes = workspace.numel() * workspace.element_size()
@@ -176,26 +188,38 @@ class Plan:
 
 
 def extend_plan(plan: Plan, desc: KVDesc, req_idx, prefix_len, extend_len, group_of_req=None,
-                group_prefix_len=None):
+                group_prefix_len=None, group_parent=None):
+    """rx_extend_plan, or rx_extend_plan_tree when group_parent is given."""
     ri, rip = _host_i32(req_idx)
     pl, plp = _host_i32(prefix_len)
     el, elp = _host_i32(extend_len)
     g, gp_ = _host_i32(group_of_req)
     gl, glp = _host_i32(group_prefix_len)
+    pa, pap = _host_i32(group_parent)
     ng = 0 if gl is None else int(gl.shape[0])
-    _check(lib().rx_extend_plan(plan.handle, C.byref(desc), int(ri.shape[0]), rip, plp, elp, gp_,
-                                ng, glp))
+    if pa is None:
+        _check(lib().rx_extend_plan(plan.handle, C.byref(desc), int(ri.shape[0]), rip, plp, elp,
+                                    gp_, ng, glp))
+    else:
+        _check(lib().rx_extend_plan_tree(plan.handle, C.byref(desc), int(ri.shape[0]), rip, plp,
+                                         elp, gp_, ng, glp, pap))
 
 
 def decode_plan(plan: Plan, desc: KVDesc, req_idx, seq_len, group_of_req=None,
-                group_prefix_len=None):
+                group_prefix_len=None, group_parent=None):
+    """rx_decode_plan, or rx_decode_plan_tree when group_parent is given."""
     ri, rip = _host_i32(req_idx)
     sl, slp = _host_i32(seq_len)
     g, gp_ = _host_i32(group_of_req)
     gl, glp = _host_i32(group_prefix_len)
+    pa, pap = _host_i32(group_parent)
     ng = 0 if gl is None else int(gl.shape[0])
-    _check(lib().rx_decode_plan(plan.handle, C.byref(desc), int(ri.shape[0]), rip, slp, gp_, ng,
-                                glp))
+    if pa is None:
+        _check(lib().rx_decode_plan(plan.handle, C.byref(desc), int(ri.shape[0]), rip, slp, gp_,
+                                    ng, glp))
+    else:
+        _check(lib().rx_decode_plan_tree(plan.handle, C.byref(desc), int(ri.shape[0]), rip, slp,
+                                         gp_, ng, glp, pap))
 
 
 def _nbytes(t) -> int:

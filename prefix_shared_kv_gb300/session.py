@@ -73,7 +73,7 @@ class DeviceWorkload:
                 e = st.extend
                 ds.ext_plan = rx.Plan()
                 rx.extend_plan(ds.ext_plan, self.desc, e.req_idx, e.prefix_len, e.extend_len,
-                               e.group_of_req, e.group_prefix_len)
+                               e.group_of_req, e.group_prefix_len, e.group_parent)
                 ds.ext_ws = workspace(ds.ext_plan.workspace_size(), self.device)
                 ds.ext_plan.upload(ds.ext_ws, stream=stream)
                 ds.ext_q = to_bf16(e.q, self.device)
@@ -84,7 +84,7 @@ class DeviceWorkload:
                 dc = st.decode
                 ds.dec_plan = rx.Plan()
                 rx.decode_plan(ds.dec_plan, self.desc, dc.req_idx, dc.seq_len, dc.group_of_req,
-                               dc.group_prefix_len)
+                               dc.group_prefix_len, dc.group_parent)
                 ds.dec_ws = workspace(ds.dec_plan.workspace_size(), self.device)
                 ds.dec_plan.upload(ds.dec_ws, stream=stream)
                 ds.dec_q = to_bf16(dc.q, self.device)

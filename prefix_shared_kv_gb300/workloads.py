@@ -72,6 +72,7 @@ class ExtendBatch:
     group_of_req: np.ndarray     # int32 [B]   -1 = no declared shared prefix
     group_prefix_len: np.ndarray  # int32 [G]
     tokens: List[np.ndarray] = field(default_factory=list)  # full token ids per request
+    group_parent: Optional[np.ndarray] = None  # int32 [G], -1 = root; None = one level
 
 
 @dataclass
@@ -81,6 +82,7 @@ class DecodeBatch:
     q: np.ndarray                # uint16 [B, Hq, d]
     group_of_req: np.ndarray     # int32 [B]
     group_prefix_len: np.ndarray  # int32 [G]
+    group_parent: Optional[np.ndarray] = None  # int32 [G], -1 = root; None = one level
 
 
 @dataclass
@@ -173,18 +175,20 @@ class Builder:
                 vn = kn.copy()
             e = d = None
             if ext is not None:
-                rows, pl, el, grp, gpl, toks = ext
+                rows, pl, el, grp, gpl, toks = ext[:6]
+                epar = np.asarray(ext[6], np.int32) if len(ext) > 6 else None
                 el = np.asarray(el, np.int32)
                 cu = np.zeros(len(el) + 1, np.int32)
                 cu[1:] = np.cumsum(el)
                 e = ExtendBatch(row_perm[np.asarray(rows, np.int64)].astype(np.int32),
                                 np.asarray(pl, np.int32), el, cu, self.q(int(cu[-1])),
-                                np.asarray(grp, np.int32), np.asarray(gpl, np.int32), toks)
+                                np.asarray(grp, np.int32), np.asarray(gpl, np.int32), toks, epar)
             if dec is not None:
-                rows, sl, grp, gpl = dec
+                rows, sl, grp, gpl = dec[:4]
+                dpar = np.asarray(dec[4], np.int32) if len(dec) > 4 else None
                 d = DecodeBatch(row_perm[np.asarray(rows, np.int64)].astype(np.int32),
                                 np.asarray(sl, np.int32), self.q(len(rows)),
-                                np.asarray(grp, np.int32), np.asarray(gpl, np.int32))
+                                np.asarray(grp, np.int32), np.asarray(gpl, np.int32), dpar)
             steps.append(Step(slots, kn, vn, e, d))
         return Workload(name, self.hq, self.hkv, self.d, 1.0 / float(np.sqrt(self.d)),
                         self.pool_size, r2t, self.k_pool, self.v_pool, steps,
@@ -299,6 +303,79 @@ def decode_workload(seed: int, num_q_heads: int, num_kv_heads: int, *, n_groups:
     return b.finish(name, [(new_runs, None, (rows, sl, grp, gpl))], cached_seqs, recipe)
 
 
+def tree_workload(seed: int, num_q_heads: int, num_kv_heads: int, *, depth: int, fanout: int,
+                  seg_lo: int, seg_hi: int, p_empty: float, n_decode: int, tail_hi: int,
+                  n_extend: int, own_hi: int, ext_lo: int, ext_hi: int,
+                  name: str = "tree") -> Workload:
+    """A random radix tree of cached segments (a node's segment U[seg_lo, seg_hi] tokens, empty
+    with probability p_empty; 1..fanout children per node down to `depth` levels) declared as a
+    group forest.  Decode requests sit on random nodes with U[0, tail_hi] cached tokens of their
+    own plus the current token; extend requests sit on random nodes with U[0, own_hi] cached tokens
+    of their own and U[ext_lo, ext_hi] new ones."""
+    rng = np.random.default_rng(seed)
+    parent, seg_len = [-1], [int(rng.integers(seg_lo, seg_hi + 1))]
+    frontier = [0]
+    for _ in range(depth - 1):
+        nxt = []
+        for nd in frontier:
+            for _ in range(int(rng.integers(1, fanout + 1))):
+                parent.append(nd)
+                seg_len.append(0 if rng.random() < p_empty else int(rng.integers(seg_lo, seg_hi + 1)))
+                nxt.append(len(parent) - 1)
+        frontier = nxt
+    n_nodes = len(parent)
+    dec_node = rng.integers(0, n_nodes, size=n_decode)
+    dec_tail = rng.integers(0, tail_hi + 1, size=n_decode)
+    ext_node = rng.integers(0, n_nodes, size=n_extend)
+    ext_own = rng.integers(0, own_hi + 1, size=n_extend)
+    ext_new = rng.integers(ext_lo, ext_hi + 1, size=n_extend)
+    need = sum(seg_len) + int(dec_tail.sum()) + n_decode + int(ext_own.sum()) + int(ext_new.sum())
+    P = max(4096, 1 << int(np.ceil(np.log2(need * 1.25 + 1))))
+    b = Builder(rng, num_q_heads, num_kv_heads, P)
+    runs = [b.cached(n) if n > 0 else None for n in seg_len]
+    plen = []
+    for nd in range(n_nodes):
+        plen.append((plen[parent[nd]] if parent[nd] >= 0 else 0) + seg_len[nd])
+
+    def path(nd):
+        out = []
+        while nd >= 0:
+            if runs[nd] is not None:
+                out.append(runs[nd])
+            nd = parent[nd]
+        return out[::-1]
+
+    cached_seqs = [(_tokens(path(nd)), _slots(path(nd))) for nd in range(n_nodes) if plen[nd] > 0]
+    new_runs = []
+    e_rows, e_pl, e_el, e_grp, e_toks = [], [], [], [], []
+    for i in range(n_extend):
+        nd = int(ext_node[i])
+        rr = path(nd) + ([b.cached(int(ext_own[i]))] if ext_own[i] > 0 else [])
+        nr = b.new(int(ext_new[i]))
+        new_runs.append(nr)
+        e_rows.append(b.row(rr + [nr]))
+        e_pl.append(plen[nd] + int(ext_own[i]))
+        e_el.append(int(ext_new[i]))
+        e_grp.append(nd)
+        e_toks.append(_tokens(rr + [nr]))
+    d_rows, d_sl, d_grp = [], [], []
+    for i in range(n_decode):
+        nd = int(dec_node[i])
+        rr = path(nd) + ([b.cached(int(dec_tail[i]))] if dec_tail[i] > 0 else [])
+        cur = b.new(1)
+        new_runs.append(cur)
+        d_rows.append(b.row(rr + [cur]))
+        d_sl.append(plen[nd] + int(dec_tail[i]) + 1)
+        d_grp.append(nd)
+    step = (new_runs, (e_rows, e_pl, e_el, e_grp, plen, e_toks, parent) if n_extend else None,
+            (d_rows, d_sl, d_grp, plen, parent) if n_decode else None)
+    recipe = (f"seed {seed}; Hq={num_q_heads} Hkv={num_kv_heads} d=128; radix tree of {n_nodes} "
+              f"nodes, depth {depth}, fanout 1..{fanout}, segments U[{seg_lo},{seg_hi}] (empty "
+              f"with p={p_empty}); {n_decode} decode on random nodes, tail U[0,{tail_hi}] + current; "
+              f"{n_extend} extend, own U[0,{own_hi}], new U[{ext_lo},{ext_hi}]; pool {P} slots")
+    return b.finish(name, [step], cached_seqs, recipe)
+
+
 # --------------------------------------------------------------------------------------------
 # The five named workloads.
 # --------------------------------------------------------------------------------------------
@@ -341,10 +418,13 @@ def llama3_gqa_decode(seed: int = 1004) -> Workload:
                            dist_hi=1000, min_pool=409600, name="llama3-gqa-decode-16x16-p16000")
 
 
-def radix_mixed(seed: int = 1005) -> Workload:
+def radix_mixed(seed: int = 1005, tree: bool = True) -> Workload:
     """Radix tree 1000 -> 8 x 500 -> 4 x 200 per branch (32 leaves).  One step: 16 leaf requests
     extend 64 tokens; 8 cache misses run a 1500-token full prefill; 40 decode requests, request j on
-    leaf j mod 32 with its own tail of U[1,32] tokens (the last one current)."""
+    leaf j mod 32 with its own tail of U[1,32] tokens (the last one current).
+    tree=True declares the radix tree as groups (root = system prompt, 8 branch nodes, 32 leaf
+    nodes for decode; extend requests belong to their branch node); tree=False declares only the
+    system prompt, one level."""
     rng = np.random.default_rng(seed)
     tails = rng.integers(1, 33, size=40)
     b = Builder(rng, 32, 32, 32768)
@@ -377,12 +457,23 @@ def radix_mixed(seed: int = 1005) -> Workload:
         new_runs.append(cur)
         d_rows.append(b.row(runs + [cur]))
         d_sl.append(1700 + int(tails[j]))
-    step = (new_runs, (e_rows, e_pl, e_el, e_grp, [1000], e_toks),
-            (d_rows, d_sl, [0] * 40, [1000]))
-    return b.finish("radix-mixed-1000-8x500-32x200", [step], cached_seqs,
+    if tree:
+        # groups: 0 root [0,1000), 1..8 branch b [1000,1500), 9..40 leaf k [1500,1700)
+        gpl = [1000] + [1500] * 8 + [1700] * 32
+        par = [-1] + [0] * 8 + [1 + k // 4 for k in range(32)]
+        e_spec = (e_rows, e_pl, e_el, [1 + k // 4 for k in range(16)] + [-1] * 8, gpl, e_toks, par)
+        d_spec = (d_rows, d_sl, [9 + j % 32 for j in range(40)], gpl, par)
+    else:
+        e_spec = (e_rows, e_pl, e_el, e_grp, [1000], e_toks)
+        d_spec = (d_rows, d_sl, [0] * 40, [1000])
+    step = (new_runs, e_spec, d_spec)
+    return b.finish("radix-mixed-1000-8x500-32x200" + ("" if tree else "-1level"), [step],
+                    cached_seqs,
                     f"seed {seed}; Hq=Hkv=32 d=128; tree 1000 -> 8x500 -> 32x200; 16 extend "
                     f"(p=1700, E=64) + 8 miss (p=0, E=1500) + 40 decode (tail U[1,32]); "
-                    f"shared-prefix groups at the 1000-token system prompt; pool 32768 slots")
+                    + ("groups = the radix tree (system prompt, branches, leaves)" if tree else
+                       "shared-prefix groups at the 1000-token system prompt only")
+                    + "; pool 32768 slots")
 
 
 NAMED = {
@@ -391,4 +482,5 @@ NAMED = {
     "decode": llama7b_decode_hf,
     "gqa-decode": llama3_gqa_decode,
     "radix-mixed": radix_mixed,
+    "radix-mixed-1level": lambda: radix_mixed(tree=False),
 }

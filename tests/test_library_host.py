@@ -141,3 +141,82 @@ def test_plans_size_workspaces_without_a_gpu(librx):
     with pytest.raises(rx.RxError) as e:
         rx.decode_attn(p, d, 16, 16, 16, 16, 16, None, stream=0)
     assert e.value.status == rx.RX_ERR_INVALID
+
+
+def test_tree_plan_argument_checks(librx):
+    p = rx.Plan()
+    d = _desc()
+    with pytest.raises(rx.RxError) as e:   # parent listed after its child
+        rx.decode_plan(p, d, [0, 1], [20, 20], [0, 1], [5, 10], [1, -1])
+    assert e.value.status == rx.RX_ERR_RANGE
+    with pytest.raises(rx.RxError) as e:   # a child's prefix shorter than its parent's
+        rx.decode_plan(p, d, [0, 1], [20, 20], [1, 1], [10, 5], [-1, 0])
+    assert e.value.status == rx.RX_ERR_RANGE
+    with pytest.raises(rx.RxError) as e:
+        rx.extend_plan(p, d, [0], [10], [3], [1], [4, 12], [-1, 0])  # prefix 12 > prefix_len 10
+    assert e.value.status == rx.RX_ERR_RANGE
+
+
+def _tree_reads(wl, max_tok):
+    """(key, KV head) rows a tree decode plan must read: each node's own keys once per member
+    tile of the requests beneath it, each request's keys past its node's prefix once."""
+    dc = wl.steps[0].decode
+    par, plen = dc.group_parent, dc.group_prefix_len
+    members = np.zeros(len(par), np.int64)
+    for g in dc.group_of_req:
+        while g >= 0:
+            members[g] += 1
+            g = par[g]
+    rows = 0
+    for g in range(len(par)):
+        lo = plen[par[g]] if par[g] >= 0 else 0
+        if members[g]:
+            rows += (plen[g] - lo) * -(-members[g] // max_tok)
+    rows += int(np.sum(dc.seq_len - plen[dc.group_of_req]))
+    return rows * wl.num_kv_heads
+
+
+def test_tree_decode_plan_reads_each_node_once(librx):
+    from prefix_shared_kv_gb300 import workloads as W
+    for seed, hq, hkv, n_dec in [(31, 8, 8, 40), (32, 8, 2, 12), (33, 32, 32, 100)]:
+        wl = W.tree_workload(seed, hq, hkv, depth=4, fanout=3, seg_lo=1, seg_hi=200, p_empty=0.2,
+                             n_decode=n_dec, tail_hi=50, n_extend=0, own_hi=0, ext_lo=1, ext_hi=1)
+        dc = wl.steps[0].decode
+        desc = rx.KVDesc(hq, hkv, 128, 128 ** -0.5, wl.pool_size, 0x1000, wl.req_to_token.shape[0],
+                         wl.req_to_token.shape[1])
+        p = rx.Plan()
+        rx.decode_plan(p, desc, dc.req_idx, dc.seq_len, dc.group_of_req, dc.group_prefix_len,
+                       dc.group_parent)
+        max_tok = 64 // (hq // hkv)
+        assert p.key_reads() == _tree_reads(wl, max_tok)
+        # with every node's requests in one member tile this is the distinct slots, each read once
+        slots = np.concatenate([wl.req_to_token[r, :n] for r, n in zip(dc.req_idx, dc.seq_len)])
+        if n_dec <= max_tok:
+            assert p.key_reads() == np.unique(slots).size * hkv
+        one = rx.Plan()
+        rx.decode_plan(one, desc, dc.req_idx, dc.seq_len)
+        assert one.key_reads() == int(dc.seq_len.sum()) * hkv
+
+
+def test_radix_mixed_tree_plans(librx):
+    from prefix_shared_kv_gb300 import workloads as W
+    wl, wl1 = W.NAMED["radix-mixed"](), W.NAMED["radix-mixed-1level"]()
+    reads = []
+    for w in (wl, wl1):
+        dc, e = w.steps[0].decode, w.steps[0].extend
+        desc = rx.KVDesc(32, 32, 128, 128 ** -0.5, w.pool_size, 0x1000, w.req_to_token.shape[0],
+                         w.req_to_token.shape[1])
+        p = rx.Plan()
+        rx.decode_plan(p, desc, dc.req_idx, dc.seq_len, dc.group_of_req, dc.group_prefix_len,
+                       dc.group_parent)
+        pe = rx.Plan()
+        rx.extend_plan(pe, desc, e.req_idx, e.prefix_len, e.extend_len, e.group_of_req,
+                       e.group_prefix_len, e.group_parent)
+        reads.append((p.key_reads(), pe.key_reads()))
+    slots = np.concatenate([wl.req_to_token[r, :n] for r, n in zip(wl.steps[0].decode.req_idx,
+                                                                 wl.steps[0].decode.seq_len)])
+    # the tree plan reads the tree's distinct KV once: 1000 + 8 x 500 + 32 x 200 + tails
+    assert reads[0][0] == np.unique(slots).size * 32
+    assert reads[1][0] > 2 * reads[0][0]
+    # extend: branch-level packing walks fewer keys than packing at the system prompt
+    assert reads[0][1] < reads[1][1]

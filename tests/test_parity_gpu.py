@@ -190,10 +190,57 @@ def test_decode_grouping_does_not_change_the_result(cuda):
 
 
 # ---------------------------------------------------------------------------------------------
+# Prefix trees (rx_decode_plan_tree / rx_extend_plan_tree): every node read once for the requests
+# beneath it, partials of all levels merged; the result is the plain definition's.
+# ---------------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("seed,hq,hkv,depth,fanout,p_empty", [
+    (21, 8, 8, 3, 3, 0.0),     # MHA, bushy
+    (22, 8, 2, 4, 3, 0.3),     # GQA 4, empty node segments
+    (23, 32, 8, 6, 1, 0.2),    # a chain six levels deep
+    (24, 16, 2, 3, 4, 0.5),    # GQA 8, many empty nodes
+])
+def test_tree_decode_and_extend(cuda, seed, hq, hkv, depth, fanout, p_empty):
+    wl = W.tree_workload(seed, hq, hkv, depth=depth, fanout=fanout, seg_lo=1, seg_hi=150,
+                         p_empty=p_empty, n_decode=40, tail_hi=90, n_extend=10, own_hi=60,
+                         ext_lo=1, ext_hi=140)
+    run_and_check(wl, cuda)
+
+
+def test_tree_decode_many_members_per_node(cuda):
+    # 150 decode requests under a 3-node chain: the root has more members than one member tile
+    wl = W.tree_workload(25, 32, 32, depth=3, fanout=1, seg_lo=200, seg_hi=1500, p_empty=0.0,
+                         n_decode=150, tail_hi=40, n_extend=0, own_hi=0, ext_lo=1, ext_hi=1)
+    run_and_check(wl, cuda)
+
+
+def test_tree_and_one_level_plans_agree(cuda):
+    wl = W.tree_workload(26, 16, 4, depth=4, fanout=2, seg_lo=30, seg_hi=300, p_empty=0.1,
+                         n_decode=30, tail_hi=60, n_extend=0, own_hi=0, ext_lo=1, ext_hi=1)
+    dw = DeviceWorkload(wl, cuda)
+    dw.run_step(0)
+    d = wl.steps[0].decode
+    plan = rx.Plan()
+    rx.decode_plan(plan, dw.desc, d.req_idx, d.seq_len)          # no groups declared
+    assert plan.key_reads() > dw.steps[0].dec_plan.key_reads()
+    ws = torch.empty(plan.workspace_size(), dtype=torch.uint8, device=cuda)
+    plan.upload(ws)
+    o2 = torch.empty_like(dw.steps[0].dec_o)
+    l2 = torch.empty_like(dw.steps[0].dec_lse)
+    rx.decode_attn(plan, dw.desc, dw.k_pool, dw.v_pool, dw.steps[0].dec_q, o2, l2, ws)
+    torch.cuda.synchronize()
+    a = A.bf16_to_f64(bits_of(o2))
+    b = A.bf16_to_f64(bits_of(dw.steps[0].dec_o))
+    assert np.abs(a - b).max() <= MAX_ABS
+    assert (l2 - dw.steps[0].dec_lse).abs().max().item() <= LSE_ABS
+
+
+# ---------------------------------------------------------------------------------------------
 # Full-size workloads in the benchmark's configuration, sampled requests.
 # ---------------------------------------------------------------------------------------------
 
-@pytest.mark.parametrize("name", ["extend", "decode", "gqa-decode", "radix-mixed"])
+@pytest.mark.parametrize("name", ["extend", "decode", "gqa-decode", "radix-mixed",
+                                  "radix-mixed-1level"])
 def test_full_size_workloads_sampled(cuda, name):
     wl = W.NAMED[name]()
     run_and_check(wl, cuda, sample=6, seed=1)
