@@ -202,8 +202,8 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["rx", "reference"], default="rx")
-    ap.add_argument("--workload", default="radix-mixed",
-                    choices=sorted(W.NAMED))
+    from prefix_shared_kv_gb300 import workloads as W
+    ap.add_argument("--workload", default="radix-mixed", choices=sorted(W.NAMED))
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", choices=["store", "extend", "decode"], default=None,

@@ -12,7 +12,8 @@
 // ring (the head block of a token is a contiguous run of HB*256 bytes), score with
 // mma.m16n8k16 (bf16 in, fp32 accumulate), keep an online softmax in registers (quad shuffles)
 // and leave a normalised partial output + base-2 log-sum-exp per (KV head, row).  A second pass
-// merges a request's partials: lse = log2 sum 2^lse_i, o = sum 2^(lse_i - lse) o_i.
+// (one warp per request and query head) merges a request's partials:
+// lse = log2 sum 2^lse_i, o = sum 2^(lse_i - lse) o_i.
 #include <cuda_runtime.h>
 #include <math_constants.h>
 
@@ -244,46 +245,46 @@ __global__ void __launch_bounds__(kThreads, 1) decode_partial_kernel(DecParams p
   }
 }
 
-// One CTA per request, one warp per query head at a time; lane owns 4 of the 128 columns.
-__global__ void __launch_bounds__(128) decode_merge_kernel(
+// One warp per (request, query head), eight to a CTA; lane owns 4 of the 128 columns.  One pass
+// over the request's partials with a running maximum: acc and tot are rescaled when it grows.
+constexpr int kMergeWarps = 8;
+__global__ void __launch_bounds__(32 * kMergeWarps) decode_merge_kernel(
     const float* __restrict__ part_o, const float* __restrict__ part_lse,
-    const int32_t* __restrict__ merge_idx, const DecMergeRef* __restrict__ refs, int hq, int gq,
-    __nv_bfloat16* __restrict__ o, float* __restrict__ lse) {
-  const int b = blockIdx.x;
-  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int32_t* __restrict__ merge_idx, const DecMergeRef* __restrict__ refs, int batch, int hq,
+    int gq, __nv_bfloat16* __restrict__ o, float* __restrict__ lse) {
+  const int64_t task = (int64_t)blockIdx.x * kMergeWarps + threadIdx.x / 32;
+  if (task >= (int64_t)batch * hq) return;
+  const int lane = threadIdx.x % 32;
+  const int b = (int)(task / hq), h = (int)(task % hq);
+  const int hk = h / gq, g = h % gq;
   const int r_begin = merge_idx[b], r_end = merge_idx[b + 1];
-  for (int h = warp; h < hq; h += 4) {
-    const int hk = h / gq, g = h % gq;
-    float mx = -CUDART_INF_F;
-    for (int i = r_begin; i < r_end; ++i) {
-      const DecMergeRef rf = refs[i];
-      mx = fmaxf(mx, part_lse[(int64_t)rf.part + (int64_t)hk * rf.rows_real + rf.row + g]);
-    }
-    const float base = (mx == -CUDART_INF_F) ? 0.f : mx;
-    float tot = 0.f;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int i = r_begin; i < r_end; ++i) {
-      const DecMergeRef rf = refs[i];
-      const int64_t idx = (int64_t)rf.part + (int64_t)hk * rf.rows_real + rf.row + g;
-      const float w = fast_exp2(part_lse[idx] - base);
-      const float4 v = *reinterpret_cast<const float4*>(part_o + idx * kHeadDim + lane * 4);
-      tot += w;
-      acc.x += w * v.x;
-      acc.y += w * v.y;
-      acc.z += w * v.z;
-      acc.w += w * v.w;
-    }
-    const float inv = tot > 0.f ? 1.f / tot : 0.f;
-    __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
-    __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
-    uint2 packed;
-    packed.x = *reinterpret_cast<uint32_t*>(&lo);
-    packed.y = *reinterpret_cast<uint32_t*>(&hi);
-    *reinterpret_cast<uint2*>(o + ((int64_t)b * hq + h) * kHeadDim + lane * 4) = packed;
-    if (lane == 0)
-      lse[(int64_t)b * hq + h] =
-          tot > 0.f ? (mx + __log2f(tot)) * 0.69314718055994530942f : -CUDART_INF_F;
+  float mx = -CUDART_INF_F, tot = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int i = r_begin; i < r_end; ++i) {
+    const DecMergeRef rf = refs[i];
+    const int64_t idx = (int64_t)rf.part + (int64_t)hk * rf.rows_real + rf.row + g;
+    const float li = part_lse[idx];
+    if (li == -CUDART_INF_F) continue;  // an empty partition contributes nothing
+    const float4 v = *reinterpret_cast<const float4*>(part_o + idx * kHeadDim + lane * 4);
+    const float m_new = fmaxf(mx, li);
+    const float a = fast_exp2(mx - m_new), w = fast_exp2(li - m_new);  // exp2(-inf) = 0
+    tot = tot * a + w;
+    acc.x = acc.x * a + w * v.x;
+    acc.y = acc.y * a + w * v.y;
+    acc.z = acc.z * a + w * v.z;
+    acc.w = acc.w * a + w * v.w;
+    mx = m_new;
   }
+  const float inv = tot > 0.f ? 1.f / tot : 0.f;
+  __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+  __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+  uint2 packed;
+  packed.x = *reinterpret_cast<uint32_t*>(&lo);
+  packed.y = *reinterpret_cast<uint32_t*>(&hi);
+  *reinterpret_cast<uint2*>(o + ((int64_t)b * hq + h) * kHeadDim + lane * 4) = packed;
+  if (lane == 0)
+    lse[(int64_t)b * hq + h] =
+        tot > 0.f ? (mx + __log2f(tot)) * 0.69314718055994530942f : -CUDART_INF_F;
 }
 
 }  // namespace
@@ -317,13 +318,24 @@ int launch_decode(const rx_kv_desc* d, const PlanHeader* h, const void* k_pool,
   p.pool_size = d->pool_size;
   p.status = reinterpret_cast<int32_t*>(base + offsetof(PlanHeader, status));
   cudaStream_t s = (cudaStream_t)stream;
+  if (h->n_xitems > 0) {  // shared-prefix units with many query rows: tensor-core kernel
+    const int e = launch_attn_items(
+        d, reinterpret_cast<const ExtItem*>(base + h->off_xitems),
+        reinterpret_cast<const ExtRow*>(base + h->off_xrows),
+        reinterpret_cast<const ExtSeg*>(base + h->off_xsegs), h->n_xitems, k_pool, v_pool, q,
+        nullptr, nullptr, p.part_o, p.part_lse, p.status, stream);
+    if (e) return e;
+  }
   if (h->n_items > 0)
     decode_partial_kernel<<<h->n_items, kThreads, kDecSmemBytes, s>>>(p);
-  if (h->batch > 0)
-    decode_merge_kernel<<<h->batch, 128, 0, s>>>(
+  if (h->batch > 0) {
+    const int64_t tasks = (int64_t)h->batch * p.hq;
+    decode_merge_kernel<<<(unsigned)((tasks + kMergeWarps - 1) / kMergeWarps), 32 * kMergeWarps, 0,
+                          s>>>(
         p.part_o, p.part_lse, reinterpret_cast<const int32_t*>(base + h->off_merge_idx),
-        reinterpret_cast<const DecMergeRef*>(base + h->off_merge), p.hq, p.gq,
+        reinterpret_cast<const DecMergeRef*>(base + h->off_merge), h->batch, p.hq, p.gq,
         static_cast<__nv_bfloat16*>(o), lse);
+  }
   return (int)cudaGetLastError();
 }
 

@@ -60,6 +60,8 @@ struct ExtParams {
   int64_t pool_size;
   int32_t* status;
   int32_t oob_row;  // a row index past the end of the pool's [pool_size * Hkv, 128] view
+  float* part_o;    // non-null: write fp32 partial rows (decode shared-prefix units)
+  float* part_lse;
 };
 
 constexpr int kN = 64;                 // keys per step
@@ -235,6 +237,7 @@ __device__ __forceinline__ void producer(const ExtParams& p, const ExtItem& it,
 // operation until the tensor pipe has taken the MMAs before it, so every wait comes first.
 __device__ __forceinline__ void mma_issuer(const ExtParams& p, int x, int ntiles, uint32_t base,
                                            uint32_t tmem, volatile int* abort) {
+  if (ntiles < 0) return;  // no tile x in this item
   constexpr uint32_t idS = tc::idesc_bf16(128, kN, false, false);
   constexpr uint32_t idO = tc::idesc_bf16(128, 128, false, true);
   const uint32_t bar = base + kOffBar;
@@ -338,9 +341,13 @@ __device__ __forceinline__ float row_exp(const uint32_t (&sr)[2][32], float sl2,
   return (a0 + a1) + (b0 + b1);
 }
 
+// TWO: tile B present, the tiles take turns for the exponentials (a compile-time choice: a runtime
+// test inside the step loop costs a few percent)
+template <bool TWO>
 __device__ __forceinline__ void softmax_rows(const ExtParams& p, const ExtItem& it,
                                              const ExtSeg* segs, int ntiles, uint32_t base,
                                              uint32_t tmem, volatile int* abort) {
+  constexpr bool two = TWO;
   const int x = threadIdx.x >> 7;   // tile: 0 = A, 1 = B
   const int r = threadIdx.x & 127;  // query row of the tile == TMEM lane
   const int wq = (threadIdx.x >> 5) & 3;
@@ -375,6 +382,7 @@ __device__ __forceinline__ void softmax_rows(const ExtParams& p, const ExtItem& 
   TileIter cur{0, segs[0].k_begin};
   bool ok = true;
   if (x == 1 && ntiles > 0) tc::mbar_arrive(bar + 8 * B_TURN);  // tile A goes first
+  // (a lone tile A takes no turns)
   for (int t = 0; t < ntiles; ++t) {
     const uint32_t col_s = col_s_of(x, t & 1);
     const bool w_ok = tc::mbar_wait(bar + 8 * (B_S_FULL + 2 * x + (t & 1)), (t >> 1) & 1, abort,
@@ -392,7 +400,7 @@ __device__ __forceinline__ void softmax_rows(const ExtParams& p, const ExtItem& 
     tc::ld32(lane_t + col_s, sr[0]);
     tc::ld32(lane_t + col_s + 32, sr[1]);
     tc::wait_ld();
-    const bool turn = tc::mbar_wait(bar + 8 * (B_TURN + x), t & 1, abort, p.status, kWaitNs);
+    const bool turn = !two || tc::mbar_wait(bar + 8 * (B_TURN + x), t & 1, abort, p.status, kWaitNs);
     if (__any_sync(0xffffffffu, !turn)) {
       ok = false;
       break;
@@ -414,7 +422,7 @@ __device__ __forceinline__ void softmax_rows(const ExtParams& p, const ExtItem& 
     // a row that has seen no visible key yet has m_used = -inf and only masked keys: any finite
     // reference gives p = 0 for them
     l = l * alpha + row_exp(sr, sl2, m_used == -CUDART_INF_F ? 0.f : m_used, pk);
-    if (x == 0 || t + 1 < ntiles) tc::mbar_arrive(bar + 8 * (B_TURN + 1 - x));  // other tile's turn
+    if (two && (x == 0 || t + 1 < ntiles)) tc::mbar_arrive(bar + 8 * (B_TURN + 1 - x));  // other's turn
     if (rescale && t > 0) {
       // O_x must hold PV_x(t-1): the phase of step t+1 of S_FULL covers it, and PV_x(t) waits for
       // this step's P
@@ -446,13 +454,28 @@ __device__ __forceinline__ void softmax_rows(const ExtParams& p, const ExtItem& 
   if (__any_sync(0xffffffffu, !w_ok)) return;
   tc::fence_after();
   const float inv = l > 0.f ? 1.f / l : 0.f;
+  // final rows: bf16 O and natural-log LSE; decode shared-prefix units: fp32 partial rows and
+  // base-2 LSE for the merge (row part[x] + r, part re-read from the table)
+  const bool partial = p.part_o != nullptr;
+  int64_t prow = 0;
+  if (partial) {
+    const ExtItem& itg = p.items[blockIdx.x];
+    prow = (int64_t)__ldg(x ? &itg.part[1] : &itg.part[0]) + r;
+  }
   __nv_bfloat16* dst = p.o + ((int64_t)q_row * p.hq + qh) * kHeadDim;
+  float* pdst = p.part_o + prow * kHeadDim;
 #pragma unroll 1
   for (int q4 = 0; q4 < 4; ++q4) {
     uint32_t ov[32];
     tc::ld32(lane_t + col_o + 32 * q4, ov);
     tc::wait_ld();
-    if (valid) {
+    if (valid && partial) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        *reinterpret_cast<float4*>(pdst + 32 * q4 + 4 * j) =
+            make_float4(__uint_as_float(ov[4 * j]) * inv, __uint_as_float(ov[4 * j + 1]) * inv,
+                        __uint_as_float(ov[4 * j + 2]) * inv, __uint_as_float(ov[4 * j + 3]) * inv);
+    } else if (valid) {
       uint32_t w[16];
 #pragma unroll
       for (int j = 0; j < 16; ++j)
@@ -463,9 +486,12 @@ __device__ __forceinline__ void softmax_rows(const ExtParams& p, const ExtItem& 
             make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
     }
   }
-  if (valid)
-    p.lse[(int64_t)q_row * p.hq + qh] =
-        l > 0.f ? (m_used + __log2f(l)) * 0.69314718055994530942f : -CUDART_INF_F;
+  if (!valid) return;
+  const float lse2 = l > 0.f ? m_used + __log2f(l) : -CUDART_INF_F;
+  if (partial)
+    p.part_lse[prow] = lse2;
+  else
+    p.lse[(int64_t)q_row * p.hq + qh] = lse2 * 0.69314718055994530942f;
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -479,13 +505,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const ExtSeg* segs = p.segs + it.seg_begin;  // small, read through the L1 by every role
   volatile int* abort = reinterpret_cast<volatile int*>(sp + kOffAbort);
+  const bool two = it.n_tok[1] > 0;  // tile B present (else tile A runs alone)
   if (threadIdx.x == 0) {
     const uint32_t bar = base + kOffBar;
     for (int i = 0; i < kStages; ++i) {
       tc::mbar_init(bar + 8 * (B_K_FULL + i), 1);
-      tc::mbar_init(bar + 8 * (B_K_FREE + i), 2);
+      tc::mbar_init(bar + 8 * (B_K_FREE + i), two ? 2 : 1);
       tc::mbar_init(bar + 8 * (B_V_FULL + i), 1);
-      tc::mbar_init(bar + 8 * (B_V_FREE + i), 2);
+      tc::mbar_init(bar + 8 * (B_V_FREE + i), two ? 2 : 1);
     }
     for (int i = 0; i < 4; ++i) {
       tc::mbar_init(bar + 8 * (B_S_FULL + i), 1);
@@ -495,7 +522,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::mbar_init(bar + 8 * (B_O_DONE + x), 1);
       tc::mbar_init(bar + 8 * (B_TURN + x), 128);
     }
-    tc::mbar_init(bar + 8 * B_Q_FULL, 256);
+    tc::mbar_init(bar + 8 * B_Q_FULL, two ? 256 : 128);
     *abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -509,7 +536,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp < kWarpK) {
     tc::regs_inc<kRegsSoftmax>();
-    softmax_rows(p, it, segs, ntiles, base, tmem, abort);
+    if (two)
+      softmax_rows<true>(p, it, segs, ntiles, base, tmem, abort);
+    else if (warp < 4)
+      softmax_rows<false>(p, it, segs, ntiles, base, tmem, abort);
   } else {
     tc::regs_dec<kRegsOther>();
     if (warp < kWarpMma) {
@@ -518,7 +548,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                base + (k ? kOffK : kOffV), k ? B_K_FULL : B_V_FULL, k ? B_K_FREE : B_V_FREE,
                abort);
     } else {
-      if ((threadIdx.x & 31) == 0) mma_issuer(p, warp - kWarpMma, ntiles, base, tmem, abort);
+      const int x = warp - kWarpMma;
+      if ((threadIdx.x & 31) == 0) mma_issuer(p, x, (x == 1 && !two) ? -1 : ntiles, base, tmem, abort);
       __syncwarp();
     }
   }
@@ -557,9 +588,10 @@ int make_pool_map(CUtensorMap* map, const void* pool, const rx_kv_desc* d) {
 
 }  // namespace
 
-int launch_extend(const rx_kv_desc* d, const PlanHeader* h, const void* k_pool,
-                  const void* v_pool, const void* q, void* o, float* lse, void* ws,
-                  void* stream) {
+int launch_attn_items(const rx_kv_desc* d, const ExtItem* items, const ExtRow* rows,
+                      const ExtSeg* segs, int32_t n_items, const void* k_pool, const void* v_pool,
+                      const void* q, void* o, float* lse, float* part_o, float* part_lse,
+                      int32_t* status, void* stream) {
   static bool attr_set = false;
   if (!attr_set) {
     // The softmax warpgroups raise their register budget with what the other warpgroups give up;
@@ -574,7 +606,7 @@ int launch_extend(const rx_kv_desc* d, const PlanHeader* h, const void* k_pool,
     if (e != cudaSuccess) return (int)e;
     attr_set = true;
   }
-  uint8_t* base = static_cast<uint8_t*>(ws);
+  if (n_items == 0) return 0;
   ExtParams p;
   p.k_pool = static_cast<const __nv_bfloat16*>(k_pool);
   p.v_pool = static_cast<const __nv_bfloat16*>(v_pool);
@@ -587,19 +619,31 @@ int launch_extend(const rx_kv_desc* d, const PlanHeader* h, const void* k_pool,
   p.hkv = d->num_kv_heads;
   p.gq = d->num_q_heads / d->num_kv_heads;
   p.scale_log2 = d->softmax_scale * 1.4426950408889634f;
-  p.items = reinterpret_cast<const ExtItem*>(base + h->off_items);
-  p.rows = reinterpret_cast<const ExtRow*>(base + h->off_rows);
-  p.segs = reinterpret_cast<const ExtSeg*>(base + h->off_segs);
+  p.items = items;
+  p.rows = rows;
+  p.segs = segs;
   p.pool_size = d->pool_size;
-  p.status = reinterpret_cast<int32_t*>(base + offsetof(PlanHeader, status));
-  if (h->n_items == 0) return 0;
+  p.status = status;
+  p.part_o = part_o;
+  p.part_lse = part_lse;
   CUtensorMap k_map, v_map;
   int e = make_pool_map(&k_map, k_pool, d);
   if (!e) e = make_pool_map(&v_map, v_pool, d);
   if (e) return e;
   p.oob_row = (int32_t)(d->pool_size * d->num_kv_heads);
-  extend_tc_kernel<<<h->n_items, kThreads, kSmem, (cudaStream_t)stream>>>(p, k_map, v_map);
+  extend_tc_kernel<<<n_items, kThreads, kSmem, (cudaStream_t)stream>>>(p, k_map, v_map);
   return (int)cudaGetLastError();
+}
+
+int launch_extend(const rx_kv_desc* d, const PlanHeader* h, const void* k_pool,
+                  const void* v_pool, const void* q, void* o, float* lse, void* ws,
+                  void* stream) {
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  return launch_attn_items(d, reinterpret_cast<const ExtItem*>(base + h->off_items),
+                           reinterpret_cast<const ExtRow*>(base + h->off_rows),
+                           reinterpret_cast<const ExtSeg*>(base + h->off_segs), h->n_items, k_pool,
+                           v_pool, q, o, lse, nullptr, nullptr,
+                           reinterpret_cast<int32_t*>(base + offsetof(PlanHeader, status)), stream);
 }
 
 }  // namespace rx

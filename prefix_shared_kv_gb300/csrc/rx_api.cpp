@@ -333,10 +333,65 @@ rx_status rx_decode_plan_tree(rx_plan* plan, const rx_kv_desc* desc, int32_t bat
   };
   std::vector<std::pair<int, int>> ch;
 
+  // Shared-prefix units whose stacked query rows reach 32 per KV head run on the tensor-core
+  // attention kernel (128 / gq requests per tile, two tiles per item, one KV head per item, about
+  // 2048-key chunks); the rest on the mma.sync kernel above.
+  const bool tc_ok = (int64_t)desc->pool_size * hkv < (int64_t)INT32_MAX;
+  const int tc_tok = 128 / gq;
+  std::vector<ExtItem> xitems;
+  std::vector<ExtRow> xrows;
+  std::vector<ExtSeg> xsegs;
+  int64_t key_reads = 0;
   for (int g = 0; g < num_groups; ++g) {
     const int lo = node_lo(g), hi = group_prefix_len[g];
     const auto& mem = members[g];
     if (mem.empty() || hi <= lo) continue;
+    if (tc_ok && (int64_t)mem.size() * gq >= 32) {
+      struct XTile {
+        int row_begin, n_tok, t0;
+      };
+      std::vector<XTile> tiles;
+      for (size_t t0 = 0; t0 < mem.size(); t0 += tc_tok) {
+        const int n_tok = (int)std::min<size_t>(tc_tok, mem.size() - t0);
+        tiles.push_back({(int)xrows.size(), n_tok, (int)t0});
+        for (int i = 0; i < n_tok; ++i)
+          xrows.push_back({mem[t0 + i], INT32_MAX, mem[t0 + i], 0});
+      }
+      const int n_ch = std::max(1, (hi - lo + 1024) / 2048);
+      const int clen = ((hi - lo + n_ch - 1) / n_ch + 63) / 64 * 64;
+      for (int c0 = lo; c0 < hi; c0 += clen) {
+        const int c1 = std::min(hi, c0 + clen);
+        const int seg = (int)xsegs.size();
+        xsegs.push_back({req_idx[mem[0]], c0, c1, -1});
+        std::vector<int64_t> part(tiles.size());
+        for (size_t k = 0; k < tiles.size(); ++k) {
+          part[k] = npart;
+          npart += (int64_t)hkv * tiles[k].n_tok * gq;
+          for (int i = 0; i < tiles[k].n_tok; ++i)
+            refs[mem[tiles[k].t0 + i]].push_back(
+                {(int32_t)part[k], tiles[k].n_tok * gq, i * gq, 0});
+        }
+        for (size_t k = 0; k < tiles.size(); k += 2) {
+          const bool pair = k + 1 < tiles.size();
+          for (int h = 0; h < hkv; ++h) {
+            ExtItem it;
+            it.row_begin[0] = tiles[k].row_begin;
+            it.n_tok[0] = tiles[k].n_tok;
+            it.row_begin[1] = pair ? tiles[k + 1].row_begin : 0;
+            it.n_tok[1] = pair ? tiles[k + 1].n_tok : 0;
+            it.seg_begin = seg;
+            it.n_seg = 1;
+            it.kv_head = h;
+            it.pad = 0;
+            it.part[0] = (int32_t)(part[k] + (int64_t)h * tiles[k].n_tok * gq);
+            it.part[1] = pair ? (int32_t)(part[k + 1] + (int64_t)h * tiles[k + 1].n_tok * gq) : 0;
+            xitems.push_back(it);
+          }
+          key_reads += (int64_t)(c1 - c0) * hkv;
+        }
+      }
+      continue;
+    }
     for (size_t t0 = 0; t0 < mem.size(); t0 += max_tok) {
       const int n_tok = (int)std::min<size_t>(max_tok, mem.size() - t0);
       const int kind = kind_of_rows(n_tok * gq);
@@ -369,7 +424,6 @@ rx_status rx_decode_plan_tree(rx_plan* plan, const rx_kv_desc* desc, int32_t bat
   if (npart > (int64_t)INT32_MAX) return fail(RX_ERR_RANGE, "plan too large");
 
   std::vector<DecItem> items;
-  int64_t key_reads = 0;
   for (const Unit& u : units) {
     const int hb = hb_of(u.kind);
     for (int h = 0; h * hb < hkv; ++h)
@@ -382,6 +436,11 @@ rx_status rx_decode_plan_tree(rx_plan* plan, const rx_kv_desc* desc, int32_t bat
   };
   std::stable_sort(items.begin(), items.end(),
                    [&](const DecItem& a, const DecItem& b) { return cost(a) > cost(b); });
+
+  std::stable_sort(xitems.begin(), xitems.end(), [&](const ExtItem& a, const ExtItem& b) {
+    return xsegs[a.seg_begin].k_end - xsegs[a.seg_begin].k_begin >
+           xsegs[b.seg_begin].k_end - xsegs[b.seg_begin].k_begin;
+  });
 
   std::vector<int32_t> midx(batch + 1, 0);
   std::vector<DecMergeRef> mref;
@@ -406,6 +465,10 @@ rx_status rx_decode_plan_tree(rx_plan* plan, const rx_kv_desc* desc, int32_t bat
   h.off_segs = off;
   h.off_merge_idx = off; off = align256(off + midx.size() * 4);
   h.off_merge = off; off = align256(off + mref.size() * sizeof(DecMergeRef));
+  h.off_xitems = off; off = align256(off + xitems.size() * sizeof(ExtItem));
+  h.off_xrows = off; off = align256(off + xrows.size() * sizeof(ExtRow));
+  h.off_xsegs = off; off = align256(off + xsegs.size() * sizeof(ExtSeg));
+  h.n_xitems = (int32_t)xitems.size();
   const size_t tables = off;
   h.off_part_o = off; off = align256(off + (size_t)npart * kHeadDim * 4);
   h.off_part_lse = off; off = align256(off + (size_t)npart * 4);
@@ -417,6 +480,9 @@ rx_status rx_decode_plan_tree(rx_plan* plan, const rx_kv_desc* desc, int32_t bat
   put(plan->blob, h.off_rows, rows);
   put(plan->blob, h.off_merge_idx, midx);
   put(plan->blob, h.off_merge, mref);
+  put(plan->blob, h.off_xitems, xitems);
+  put(plan->blob, h.off_xrows, xrows);
+  put(plan->blob, h.off_xsegs, xsegs);
   plan->ws_bytes = off;
   plan->key_reads = key_reads;
   plan->kind = 2;

@@ -66,7 +66,10 @@ struct ExtSeg {
 };
 
 // Two row tiles (A, B) of the same KV head that walk the same key segments: every K/V step feeds
-// 256 query rows.  Tile B may be empty (n_tok[1] == 0).
+// 256 query rows.  Tile B may be empty (n_tok[1] == 0: the CTA runs tile A alone).  The same
+// kernel serves a decode plan's shared-prefix units with many query rows: its rows are then
+// decode requests, and each tile writes fp32 partial rows part[x] + r (row r = token * gq + g)
+// for the decode merge instead of final outputs.
 struct ExtItem {
   int32_t row_begin[2];  // into ext_rows
   int32_t n_tok[2];      // tokens per tile (rows = n_tok * gq <= 128)
@@ -74,6 +77,7 @@ struct ExtItem {
   int32_t n_seg;
   int32_t kv_head;
   int32_t pad;
+  int32_t part[2];       // decode plans: first partial row of each tile; unused for extend
 };
 
 // Workspace layout written by rx_plan_upload: a 256-byte header, then the tables, then (decode)
@@ -89,7 +93,11 @@ struct PlanHeader {
   int64_t off_items, off_rows, off_segs, off_merge_idx, off_merge, off_part_o, off_part_lse;
   int64_t n_part_rows;
   int64_t total_bytes;
-  int64_t pad[19];
+  // decode plans: shared-prefix units run by the tensor-core attention kernel (ExtItem / ExtRow /
+  // ExtSeg tables writing partial rows); n_xitems = 0 when there are none
+  int64_t off_xitems, off_xrows, off_xsegs;
+  int32_t n_xitems, pad32;
+  int64_t pad[15];
 };
 static_assert(sizeof(PlanHeader) == 256, "header is 256 bytes");
 
@@ -102,6 +110,13 @@ int launch_decode(const rx_kv_desc* d, const PlanHeader* h, const void* k_pool,
 int launch_extend(const rx_kv_desc* d, const PlanHeader* h, const void* k_pool,
                   const void* v_pool, const void* q, void* o, float* lse, void* ws,
                   void* stream);
+// The tensor-core attention kernel over `n_items` items of tables in device memory; with
+// part_o != nullptr every tile writes fp32 partial rows (normalised O, base-2 LSE) instead of o /
+// lse.  `status` is the plan's device status word.
+int launch_attn_items(const rx_kv_desc* d, const ExtItem* items, const ExtRow* rows,
+                      const ExtSeg* segs, int32_t n_items, const void* k_pool, const void* v_pool,
+                      const void* q, void* o, float* lse, float* part_o, float* part_lse,
+                      int32_t* status, void* stream);
 
 // Records `msg` as the calling thread's last error and returns `st`.
 rx_status set_error(rx_status st, const char* msg);

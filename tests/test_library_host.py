@@ -159,7 +159,9 @@ def test_tree_plan_argument_checks(librx):
 
 def _tree_reads(wl, max_tok):
     """(key, KV head) rows a tree decode plan must read: each node's own keys once per member
-    tile of the requests beneath it, each request's keys past its node's prefix once."""
+    tile of the requests beneath it, each request's keys past its node's prefix once.  A node
+    whose stacked query rows (members x gq) reach 32 runs on the tensor-core kernel: tiles of
+    128 rows, two tiles per read."""
     dc = wl.steps[0].decode
     par, plen = dc.group_parent, dc.group_prefix_len
     members = np.zeros(len(par), np.int64)
@@ -171,7 +173,9 @@ def _tree_reads(wl, max_tok):
     for g in range(len(par)):
         lo = plen[par[g]] if par[g] >= 0 else 0
         if members[g]:
-            rows += (plen[g] - lo) * -(-members[g] // max_tok)
+            gq = wl.num_q_heads // wl.num_kv_heads
+            per_read = 2 * (128 // gq) if members[g] * gq >= 32 else max_tok
+            rows += (plen[g] - lo) * -(-members[g] // per_read)
     rows += int(np.sum(dc.seq_len - plen[dc.group_of_req]))
     return rows * wl.num_kv_heads
 
@@ -189,9 +193,9 @@ def test_tree_decode_plan_reads_each_node_once(librx):
                        dc.group_parent)
         max_tok = 64 // (hq // hkv)
         assert p.key_reads() == _tree_reads(wl, max_tok)
-        # with every node's requests in one member tile this is the distinct slots, each read once
+        # with every node's requests in one read this is the distinct slots, each read once
         slots = np.concatenate([wl.req_to_token[r, :n] for r, n in zip(dc.req_idx, dc.seq_len)])
-        if n_dec <= max_tok:
+        if n_dec <= max_tok or n_dec * (hq // hkv) <= 256:
             assert p.key_reads() == np.unique(slots).size * hkv
         one = rx.Plan()
         rx.decode_plan(one, desc, dc.req_idx, dc.seq_len)
