@@ -17,6 +17,8 @@
 #include <cuda_runtime.h>
 #include <math_constants.h>
 
+#include <mutex>
+
 #include "ptx.cuh"
 #include "rx_internal.h"
 
@@ -287,6 +289,18 @@ __global__ void __launch_bounds__(32 * kMergeWarps) decode_merge_kernel(
         tot > 0.f ? (mx + __log2f(tot)) * 0.69314718055994530942f : -CUDART_INF_F;
 }
 
+// A second stream per device on which the tensor-core shared-prefix units run beside the mma.sync
+// units (fork and join through events, so the pair also works under stream capture): each kernel's
+// last wave would otherwise leave SMs idle.  Created on first use; the lock serialises the
+// record / wait sequence of concurrent callers.
+struct AuxStream {
+  cudaStream_t stream = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+constexpr int kMaxDevices = 64;
+AuxStream g_aux[kMaxDevices];
+std::mutex g_aux_lock;
+
 }  // namespace
 
 int launch_decode(const rx_kv_desc* d, const PlanHeader* h, const void* k_pool,
@@ -318,16 +332,41 @@ int launch_decode(const rx_kv_desc* d, const PlanHeader* h, const void* k_pool,
   p.pool_size = d->pool_size;
   p.status = reinterpret_cast<int32_t*>(base + offsetof(PlanHeader, status));
   cudaStream_t s = (cudaStream_t)stream;
-  if (h->n_xitems > 0) {  // shared-prefix units with many query rows: tensor-core kernel
-    const int e = launch_attn_items(
+  auto run_x = [&](cudaStream_t st) {  // shared-prefix units with many query rows: tcgen05 kernel
+    return launch_attn_items(
         d, reinterpret_cast<const ExtItem*>(base + h->off_xitems),
         reinterpret_cast<const ExtRow*>(base + h->off_xrows),
         reinterpret_cast<const ExtSeg*>(base + h->off_xsegs), h->n_xitems, k_pool, v_pool, q,
-        nullptr, nullptr, p.part_o, p.part_lse, p.status, stream);
+        nullptr, nullptr, p.part_o, p.part_lse, p.status, st);
+  };
+  if (h->n_xitems > 0 && h->n_items > 0) {
+    int dev = 0;
+    cudaError_t ce = cudaGetDevice(&dev);
+    if (ce != cudaSuccess) return (int)ce;
+    if (dev < 0 || dev >= kMaxDevices) return (int)cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_aux_lock);
+    AuxStream& a = g_aux[dev];
+    if (!a.stream) {
+      ce = cudaStreamCreateWithFlags(&a.stream, cudaStreamNonBlocking);
+      if (ce == cudaSuccess) ce = cudaEventCreateWithFlags(&a.fork, cudaEventDisableTiming);
+      if (ce == cudaSuccess) ce = cudaEventCreateWithFlags(&a.join, cudaEventDisableTiming);
+      if (ce != cudaSuccess) return (int)ce;
+    }
+    ce = cudaEventRecord(a.fork, s);
+    if (ce == cudaSuccess) ce = cudaStreamWaitEvent(a.stream, a.fork, 0);
+    if (ce != cudaSuccess) return (int)ce;
+    const int e = run_x(a.stream);
     if (e) return e;
-  }
-  if (h->n_items > 0)
     decode_partial_kernel<<<h->n_items, kThreads, kDecSmemBytes, s>>>(p);
+    ce = cudaEventRecord(a.join, a.stream);
+    if (ce == cudaSuccess) ce = cudaStreamWaitEvent(s, a.join, 0);
+    if (ce != cudaSuccess) return (int)ce;
+  } else if (h->n_xitems > 0) {
+    const int e = run_x(s);
+    if (e) return e;
+  } else if (h->n_items > 0) {
+    decode_partial_kernel<<<h->n_items, kThreads, kDecSmemBytes, s>>>(p);
+  }
   if (h->batch > 0) {
     const int64_t tasks = (int64_t)h->batch * p.hq;
     decode_merge_kernel<<<(unsigned)((tasks + kMergeWarps - 1) / kMergeWarps), 32 * kMergeWarps, 0,
