@@ -233,6 +233,42 @@ rx_status rx_radix_match(const rx_radix* tree, const int32_t* tokens, int64_t n,
 /* Number of tokens (= pool slots) the tree holds, and its node count (root excluded). */
 rx_status rx_radix_stats(const rx_radix* tree, int64_t* tokens, int64_t* nodes);
 
+/* Memory management (SGLang explainer, "LRU退避": free the least recently used leaves whose
+ * reference count is 0, recursively; SGLang paper notes, §3: nodes keep reference counts, and the
+ * cache shares one pool with the running requests; Figure 3 walks it through nine steps).
+ * Every insert and acquire advances a logical clock and stamps the nodes on its path.
+ *
+ * rx_radix_acquire: rx_radix_match of tokens[0..n) at match_unit that also stamps the saved
+ * prefix's nodes as used now (the edge at its end is split so exactly the saved tokens form
+ * nodes) and, with lock != 0, holds them (reference count + 1) until rx_radix_release of the same
+ * tokens[0..*saved).  out_slots (nullable, capacity n) receives the saved tokens' slots.
+ * rx_radix_release: drops one hold on the nodes spelling tokens[0..n); RX_ERR_INVALID (nothing
+ * changed) if they do not end on a node boundary or are not held.
+ * rx_radix_evict: frees whole nodes -- each time the least recently used leaf not held by a
+ * request (the older node first on a tie) -- until at least n_tokens slots are freed or none is
+ * left to free; a parent left without children becomes a candidate.  Freed slots go to out_slots
+ * (nullable; with a buffer, eviction stops before a node that would overflow `capacity`);
+ * *n_freed receives their number.  Insert's note still applies: the caller's slots for tokens the
+ * tree already held (the first n - new_tokens) are not taken and go back to the pool. */
+rx_status rx_radix_acquire(rx_radix* tree, const int32_t* tokens, int64_t n, int32_t match_unit,
+                           int32_t lock, int64_t* saved, int32_t* out_slots);
+rx_status rx_radix_release(rx_radix* tree, const int32_t* tokens, int64_t n);
+rx_status rx_radix_evict(rx_radix* tree, int64_t n_tokens, int32_t* out_slots, int64_t capacity,
+                         int64_t* n_freed);
+
+/* Slot pool: the pool slots that neither the cache nor a running request holds, handed out oldest
+ * freed first (slots 0..pool_size-1 at creation).  rx_slot_pool_alloc takes n slots for new tokens;
+ * when fewer are free and `tree` is given, it first evicts from the tree (rx_radix_evict) and
+ * takes the freed slots back; RX_ERR_WORKSPACE if still short (no slot taken; evicted nodes stay
+ * evicted).  rx_slot_pool_release returns slots (a finished request's tokens that the tree did
+ * not take); RX_ERR_RANGE for a slot outside the pool (nothing returned).  (host) */
+typedef struct rx_slot_pool rx_slot_pool;
+rx_status rx_slot_pool_create(int64_t pool_size, rx_slot_pool** out);
+void rx_slot_pool_destroy(rx_slot_pool* pool);
+int64_t rx_slot_pool_free_count(const rx_slot_pool* pool);
+rx_status rx_slot_pool_alloc(rx_slot_pool* pool, rx_radix* tree, int64_t n, int32_t* out_slots);
+rx_status rx_slot_pool_release(rx_slot_pool* pool, const int32_t* slots, int64_t n);
+
 /* ---------------------------------------------------------------------------------------------
  * Token accounting (host, pure functions).
  * ------------------------------------------------------------------------------------------- */

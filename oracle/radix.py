@@ -54,3 +54,148 @@ class PrefixStore:
 
     def __len__(self):
         return self._n
+
+
+class LRURadixCache:
+    """Plain model of the radix cache's memory management, for checking the library's.
+
+    Pages: SGLang explainer, "LRU退避" (when memory runs short, free the least recently accessed
+    leaves of the radix tree, recursively, starting with leaves whose reference count is 0, so
+    caches in use stay protected); SGLang paper notes §3 (LRU on leaf nodes; a node is reclaimed
+    only when its reference count is 0; the cache shares one memory pool with the running
+    requests) and Figure 3 (nine steps of inserts, reuse, splits and evictions).
+
+    Readings (the pages do not fix these details): a logical clock advances on every insert and
+    every acquire, and stamps the nodes on that call's path; an acquire splits the edge at the
+    end of the prefix it saves, so that exactly those tokens form the held nodes; among leaves of
+    equal age the node created first goes first.  The tree is a list-based radix tree; every
+    search is a linear scan.
+    """
+
+    class _Node:
+        def __init__(self, toks, slots, parent, last, nid):
+            self.toks, self.slots, self.kids = list(toks), list(slots), []
+            self.parent, self.last, self.ref, self.id = parent, last, 0, nid
+
+    def __init__(self):
+        self._clock = 0
+        self._ids = 0
+        self.root = self._Node([], [], None, 0, 0)
+
+    def _new(self, toks, slots, parent, last):
+        self._ids += 1
+        return self._Node(toks, slots, parent, last, self._ids)
+
+    def _child(self, node, tok):
+        for k in node.kids:
+            if k.toks[0] == tok:
+                return k
+        return None
+
+    def _split(self, node, c):
+        """node keeps toks[c:]; a new node with toks[:c] takes its place under its parent."""
+        inner = self._new(node.toks[:c], node.slots[:c], node.parent, node.last)
+        inner.ref = node.ref
+        pa = node.parent
+        pa.kids[pa.kids.index(node)] = inner
+        node.toks, node.slots, node.parent = node.toks[c:], node.slots[c:], inner
+        inner.kids.append(node)
+        return inner
+
+    @staticmethod
+    def _common(a, b):
+        i = 0
+        while i < len(a) and i < len(b) and a[i] == b[i]:
+            i += 1
+        return i
+
+    def _walk(self, tokens):
+        """matched token count and their slots (no changes)."""
+        node, pos, slots = self.root, 0, []
+        while pos < len(tokens):
+            k = self._child(node, tokens[pos])
+            if k is None:
+                break
+            c = self._common(tokens[pos:], k.toks)
+            slots += k.slots[:c]
+            pos += c
+            if c < len(k.toks):
+                break
+            node = k
+        return pos, slots
+
+    def insert(self, tokens, slots):
+        tokens, slots = [int(t) for t in tokens], [int(s) for s in slots]
+        self._clock += 1
+        node, pos = self.root, 0
+        while pos < len(tokens):
+            k = self._child(node, tokens[pos])
+            if k is None:
+                node.kids.append(self._new(tokens[pos:], slots[pos:], node, self._clock))
+                return len(tokens) - pos
+            c = self._common(tokens[pos:], k.toks)
+            if c < len(k.toks):
+                k = self._split(k, c)
+            k.last = self._clock
+            pos += c
+            node = k
+        return 0
+
+    def acquire(self, tokens, unit=1, lock=True):
+        tokens = [int(t) for t in tokens]
+        m, slots = self._walk(tokens)
+        s = m // unit * unit
+        self._clock += 1
+        node, pos = self.root, 0
+        while pos < s:
+            k = self._child(node, tokens[pos])
+            if s - pos < len(k.toks):
+                k = self._split(k, s - pos)
+            k.last = self._clock
+            if lock:
+                k.ref += 1
+            pos += len(k.toks)
+            node = k
+        return s, slots[:s]
+
+    def release(self, tokens):
+        tokens = [int(t) for t in tokens]
+        node, pos, path = self.root, 0, []
+        while pos < len(tokens):
+            k = self._child(node, tokens[pos])
+            if k is None or tokens[pos:pos + len(k.toks)] != k.toks or k.ref < 1:
+                raise ValueError("not a held path")
+            path.append(k)
+            pos += len(k.toks)
+            node = k
+        for k in path:
+            k.ref -= 1
+
+    def _nodes(self):
+        out, stack = [], list(self.root.kids)
+        while stack:
+            k = stack.pop()
+            out.append(k)
+            stack += k.kids
+        return out
+
+    def evict(self, n_tokens):
+        """Slots freed, in eviction order: repeatedly the least recently used unheld leaf."""
+        freed = []
+        while len(freed) < n_tokens:
+            leaves = [k for k in self._nodes() if not k.kids and k.ref == 0]
+            if not leaves:
+                break
+            k = min(leaves, key=lambda x: (x.last, x.id))
+            freed += k.slots
+            k.parent.kids.remove(k)
+        return freed
+
+    def stats(self):
+        nodes = self._nodes()
+        return sum(len(k.toks) for k in nodes), len(nodes)
+
+    def match(self, tokens, unit=1):
+        m, slots = self._walk([int(t) for t in tokens])
+        s = m // unit * unit
+        return s, slots[:s]

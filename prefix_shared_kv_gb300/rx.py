@@ -24,7 +24,9 @@ EXPORTED = [
     "rx_plan_workspace_size", "rx_plan_upload", "rx_plan_key_reads", "rx_extend_plan",
     "rx_extend_plan_tree", "rx_extend_attn", "rx_decode_plan", "rx_decode_plan_tree",
     "rx_decode_attn", "rx_decode_attn_noalloc", "rx_read_status", "rx_radix_create", "rx_radix_destroy",
-    "rx_radix_insert", "rx_radix_match", "rx_radix_stats", "rx_saved_tokens", "rx_token_saving",
+    "rx_radix_insert", "rx_radix_match", "rx_radix_stats", "rx_radix_acquire", "rx_radix_release",
+    "rx_radix_evict", "rx_slot_pool_create", "rx_slot_pool_destroy", "rx_slot_pool_free_count",
+    "rx_slot_pool_alloc", "rx_slot_pool_release", "rx_saved_tokens", "rx_token_saving",
     "rx_compute_reduction",
 ]
 
@@ -84,6 +86,14 @@ def lib():
         "rx_radix_insert": (C.c_int, [_P, _I32P, _I32P, C.c_int64, _I64P]),
         "rx_radix_match": (C.c_int, [_P, _I32P, C.c_int64, C.c_int32, _I64P, _I32P]),
         "rx_radix_stats": (C.c_int, [_P, _I64P, _I64P]),
+        "rx_radix_acquire": (C.c_int, [_P, _I32P, C.c_int64, C.c_int32, C.c_int32, _I64P, _I32P]),
+        "rx_radix_release": (C.c_int, [_P, _I32P, C.c_int64]),
+        "rx_radix_evict": (C.c_int, [_P, C.c_int64, _I32P, C.c_int64, _I64P]),
+        "rx_slot_pool_create": (C.c_int, [C.c_int64, C.POINTER(_P)]),
+        "rx_slot_pool_destroy": (None, [_P]),
+        "rx_slot_pool_free_count": (C.c_int64, [_P]),
+        "rx_slot_pool_alloc": (C.c_int, [_P, _P, C.c_int64, _I32P]),
+        "rx_slot_pool_release": (C.c_int, [_P, _I32P, C.c_int64]),
         "rx_saved_tokens": (C.c_int64, [C.c_int64, C.c_int32]),
         "rx_token_saving": (C.c_double, [C.c_int64, C.c_int64]),
         "rx_compute_reduction": (C.c_double, [C.c_int64, C.c_int64]),
@@ -292,6 +302,58 @@ class Radix:
         a, b = C.c_int64(0), C.c_int64(0)
         _check(lib().rx_radix_stats(self._h, C.byref(a), C.byref(b)))
         return a.value, b.value
+
+    def acquire(self, tokens, match_unit: int = 1, lock: bool = True):
+        """(saved tokens, their slots); with lock the saved prefix is held until release()."""
+        t, tp = _host_i32(tokens)
+        saved = C.c_int64(0)
+        out = np.zeros(max(1, t.shape[0]), np.int32)
+        _check(lib().rx_radix_acquire(self._h, tp, int(t.shape[0]), match_unit, int(bool(lock)),
+                                      C.byref(saved), out.ctypes.data_as(_I32P)))
+        return saved.value, out[:saved.value].copy()
+
+    def release(self, tokens):
+        t, tp = _host_i32(tokens)
+        _check(lib().rx_radix_release(self._h, tp, int(t.shape[0])))
+
+    def evict(self, n_tokens: int) -> np.ndarray:
+        """Slots freed by evicting least recently used unheld leaves (>= n_tokens if possible)."""
+        total, _ = self.stats()
+        out = np.zeros(max(1, total), np.int32)
+        n = C.c_int64(0)
+        _check(lib().rx_radix_evict(self._h, int(n_tokens), out.ctypes.data_as(_I32P), total,
+                                    C.byref(n)))
+        return out[:n.value].copy()
+
+
+class SlotPool:
+    """rx_slot_pool: free pool slots shared by the cache and the running requests."""
+
+    def __init__(self, pool_size: int):
+        h = _P()
+        _check(lib().rx_slot_pool_create(int(pool_size), C.byref(h)))
+        self._h = h
+
+    def __del__(self):
+        try:
+            if self._h:
+                lib().rx_slot_pool_destroy(self._h)
+                self._h = None
+        except Exception:
+            pass
+
+    def free_count(self) -> int:
+        return int(lib().rx_slot_pool_free_count(self._h))
+
+    def alloc(self, n: int, tree: Optional["Radix"] = None) -> np.ndarray:
+        out = np.zeros(max(1, n), np.int32)
+        _check(lib().rx_slot_pool_alloc(self._h, tree._h if tree is not None else None, int(n),
+                                        out.ctypes.data_as(_I32P)))
+        return out[:n].copy()
+
+    def release(self, slots):
+        s, sp = _host_i32(slots)
+        _check(lib().rx_slot_pool_release(self._h, sp, int(s.shape[0])))
 
 
 def saved_tokens(matched: int, unit: int) -> int:
