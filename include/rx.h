@@ -269,6 +269,27 @@ int64_t rx_slot_pool_free_count(const rx_slot_pool* pool);
 rx_status rx_slot_pool_alloc(rx_slot_pool* pool, rx_radix* tree, int64_t n, int32_t* out_slots);
 rx_status rx_slot_pool_release(rx_slot_pool* pool, const int32_t* slots, int64_t n);
 
+/* Cache-aware order of a batch (SGLang paper notes, §3 cache-aware scheduling and App. A.3,
+ * Theorem 3.1: with a cache holding at least the longest request, the depth-first order of the
+ * batch's radix tree computes every edge once, which maximises the cache hit rate; serving the
+ * longest shared prefix first approximates it).  Request r is tokens[offsets[r] .. offsets[r+1]);
+ * order (capacity batch) receives a permutation of 0..batch-1: a pre-order walk of the batch's
+ * radix tree, children by first token, each node's ending requests in batch order.  (host) */
+rx_status rx_dfs_order(const int32_t* tokens, const int64_t* offsets, int32_t batch,
+                       int32_t* order);
+
+/* BatchLLM group formation (BatchLLM explainer, Global Prefix Sharing, merge criterion): one-level
+ * groups for a batch from its radix tree.  gain(c') = (leaves(c') - 1) * tokens(c'), with leaves =
+ * requests in the subtree and tokens = the node's own tokens; a node c' below a group's node c
+ * starts a group of its own when gain(c') > tokens(c) (the penalty).  Reading (the page leaves
+ * the merge step open): groups start at the root's children holding >= 2 requests, the rule is
+ * applied recursively at every group's node, a request belongs to the deepest group on its path.
+ * Outputs: group_of_req[r] (-1 = no group), group_prefix_len[g] (capacity batch; nullable) =
+ * tokens from the root through g's node, *num_groups -- ready for rx_extend_plan /
+ * rx_decode_plan.  Request r is tokens[offsets[r] .. offsets[r+1]).  (host) */
+rx_status rx_gain_groups(const int32_t* tokens, const int64_t* offsets, int32_t batch,
+                         int32_t* group_of_req, int32_t* group_prefix_len, int32_t* num_groups);
+
 /* ---------------------------------------------------------------------------------------------
  * Token accounting (host, pure functions).
  * ------------------------------------------------------------------------------------------- */

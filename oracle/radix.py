@@ -199,3 +199,52 @@ class LRURadixCache:
         m, slots = self._walk([int(t) for t in tokens])
         s = m // unit * unit
         return s, slots[:s]
+
+
+def edge_tokens(sequences) -> int:
+    """Tokens on the edges of the batch's radix tree = the batch's distinct prefixes: the least a
+    batch must compute, each edge's KV once (SGLang paper notes, App. A.3, proof of Theorem 3.1)."""
+    return len({tuple(q[:i + 1]) for q in sequences for i in range(len(q))})
+
+
+def computed_tokens(sequences, order, capacity) -> int:
+    """Prefill tokens computed when the batch runs in `order` through an LRU radix cache of
+    `capacity` tokens: each request reuses its cached prefix (held while it runs), computes the
+    rest, and enters the cache, the least recently used unheld leaves making room."""
+    cache = LRURadixCache()
+    total = 0
+    slot = 0
+    for r in order:
+        q = [int(t) for t in sequences[r]]
+        hit, _ = cache.acquire(q, 1, True)
+        need = len(q) - hit
+        over = cache.stats()[0] + need - capacity
+        if over > 0:
+            cache.evict(over)
+        cache.insert(q, list(range(slot, slot + len(q))))
+        slot += len(q)
+        cache.release(q[:hit])
+        total += need
+    return total
+
+
+def longest_prefix_first(sequences, capacity):
+    """Order chosen online: next the waiting request with the longest cached prefix (ties: lower
+    index), with the cache of computed_tokens (SGLang paper notes, §3: longest-shared-prefix-first
+    instead of first-come-first-served)."""
+    cache = LRURadixCache()
+    waiting = list(range(len(sequences)))
+    order, slot = [], 0
+    while waiting:
+        best = max(waiting, key=lambda r: (cache.match(sequences[r])[0], -r))
+        waiting.remove(best)
+        order.append(best)
+        q = [int(t) for t in sequences[best]]
+        hit, _ = cache.acquire(q, 1, True)
+        over = cache.stats()[0] + len(q) - hit - capacity
+        if over > 0:
+            cache.evict(over)
+        cache.insert(q, list(range(slot, slot + len(q))))
+        slot += len(q)
+        cache.release(q[:hit])
+    return order

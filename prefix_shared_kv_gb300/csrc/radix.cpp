@@ -15,6 +15,7 @@
 // is a candidate in turn -- until enough slots are free.  The slot pool hands pool slots to the
 // new tokens of running requests and takes back what eviction frees: the cache and the running
 // requests share one pool.
+#include <algorithm>
 #include <cmath>
 #include <cstring>
 #include <deque>
@@ -280,6 +281,133 @@ rx_status rx_slot_pool_release(rx_slot_pool* pool, const int32_t* slots, int64_t
     if (slots[i] < 0 || slots[i] >= pool->size) return RX_ERR_RANGE;
   }
   for (int64_t i = 0; i < n; ++i) pool->free.push_back(slots[i]);
+  return RX_OK;
+}
+
+// Cache-aware ordering (SGLang paper notes, §3 cache-aware scheduling and App. A.3, Theorem 3.1:
+// with a cache at least as large as the longest request, running a batch in the depth-first order
+// of its radix tree computes every edge's KV once, which is optimal; longest-shared-prefix-first
+// approximates it online).  The batch's sequences go into a scratch radix tree (every sequence
+// then ends on a node boundary); a pre-order walk, children by first token, emits the requests
+// ending at each node before descending.
+rx_status rx_dfs_order(const int32_t* tokens, const int64_t* offsets, int32_t batch,
+                       int32_t* order) {
+  if (batch < 0 || (batch > 0 && (!tokens || !offsets || !order))) return RX_ERR_INVALID;
+  rx_radix tree;
+  for (int32_t r = 0; r < batch; ++r) {
+    const int64_t n = offsets[r + 1] - offsets[r];
+    if (n < 0) return RX_ERR_INVALID;
+    std::vector<int32_t> dummy((size_t)n, 0);
+    rx_status st = rx_radix_insert(&tree, tokens + offsets[r], dummy.data(), n, nullptr);
+    if (st) return st;
+  }
+  // the node each sequence ends at
+  std::unordered_map<const Node*, std::vector<int32_t>> ends;
+  for (int32_t r = 0; r < batch; ++r) {
+    const int32_t* t = tokens + offsets[r];
+    const int64_t n = offsets[r + 1] - offsets[r];
+    const Node* node = &tree.root;
+    int64_t pos = 0;
+    while (pos < n) {
+      node = node->children.find(t[pos])->second.get();
+      pos += (int64_t)node->tokens.size();
+    }
+    ends[node].push_back(r);
+  }
+  int32_t k = 0;
+  std::vector<const Node*> stack{&tree.root};
+  while (!stack.empty()) {
+    const Node* x = stack.back();
+    stack.pop_back();
+    auto it = ends.find(x);
+    if (it != ends.end())
+      for (int32_t r : it->second) order[k++] = r;
+    std::vector<const Node*> kids;
+    for (auto& kv : x->children) kids.push_back(kv.second.get());
+    std::sort(kids.begin(), kids.end(),
+              [](const Node* a, const Node* b) { return a->tokens[0] > b->tokens[0]; });
+    for (const Node* c : kids) stack.push_back(c);  // smallest first token popped first
+  }
+  return RX_OK;
+}
+
+// BatchLLM's group formation (BatchLLM explainer, Global Prefix Sharing: "マージ判定の基準"):
+// gain(c') = (leaves(c') - 1) * tokens(c') for a node c' below a group's node c; c' forms a group
+// of its own (its members share the longer prefix through c') when the gain exceeds the penalty
+// tokens(c).  Reading, as the explainer leaves the merge step open: groups start at the root's
+// children holding at least two requests, the rule is applied recursively to every node a group
+// starts at, and a request belongs to the deepest group on its path.
+rx_status rx_gain_groups(const int32_t* tokens, const int64_t* offsets, int32_t batch,
+                         int32_t* group_of_req, int32_t* group_prefix_len, int32_t* num_groups) {
+  if (batch < 0 || !num_groups || (batch > 0 && (!tokens || !offsets || !group_of_req)))
+    return RX_ERR_INVALID;
+  rx_radix tree;
+  for (int32_t r = 0; r < batch; ++r) {
+    const int64_t n = offsets[r + 1] - offsets[r];
+    if (n < 0) return RX_ERR_INVALID;
+    std::vector<int32_t> dummy((size_t)n, 0);
+    rx_status st = rx_radix_insert(&tree, tokens + offsets[r], dummy.data(), n, nullptr);
+    if (st) return st;
+  }
+  // requests ending in each node's subtree (leaves(c)), and the path of each request
+  std::unordered_map<const Node*, int64_t> leaves;
+  std::vector<std::vector<const Node*>> paths((size_t)batch);
+  for (int32_t r = 0; r < batch; ++r) {
+    const int32_t* t = tokens + offsets[r];
+    const int64_t n = offsets[r + 1] - offsets[r];
+    const Node* node = &tree.root;
+    int64_t pos = 0;
+    while (pos < n) {
+      node = node->children.find(t[pos])->second.get();
+      pos += (int64_t)node->tokens.size();
+      paths[(size_t)r].push_back(node);
+      leaves[node] += 1;
+    }
+  }
+  // nodes where a group starts, with their prefix lengths
+  std::unordered_map<const Node*, int32_t> group_at;
+  std::vector<int32_t> prefix;
+  struct Item {
+    const Node* node;
+    int64_t depth;  // tokens from the root through node
+  };
+  std::vector<Item> todo;
+  for (auto& kv : tree.root.children)
+    if (leaves[kv.second.get()] >= 2)
+      todo.push_back({kv.second.get(), (int64_t)kv.second->tokens.size()});
+  while (!todo.empty()) {
+    const Item it = todo.back();
+    todo.pop_back();
+    group_at[it.node] = (int32_t)prefix.size();
+    prefix.push_back((int32_t)it.depth);
+    // every node below it.node is a candidate c' (its path from it.node passes nodes that did
+    // not split, as those keep their requests in this group)
+    std::vector<Item> below;
+    for (auto& kv : it.node->children)
+      below.push_back({kv.second.get(), it.depth + (int64_t)kv.second->tokens.size()});
+    while (!below.empty()) {
+      const Item c = below.back();
+      below.pop_back();
+      const int64_t gain = (leaves[c.node] - 1) * (int64_t)c.node->tokens.size();
+      if (leaves[c.node] >= 2 && gain > (int64_t)it.node->tokens.size()) {
+        todo.push_back(c);
+      } else {
+        for (auto& kv : c.node->children)
+          below.push_back({kv.second.get(), c.depth + (int64_t)kv.second->tokens.size()});
+      }
+    }
+  }
+  for (int32_t r = 0; r < batch; ++r) {
+    int32_t g = -1;
+    for (const Node* x : paths[(size_t)r]) {
+      auto f = group_at.find(x);
+      if (f != group_at.end()) g = f->second;
+    }
+    group_of_req[r] = g;
+  }
+  if (group_prefix_len)
+    std::memcpy(group_prefix_len, prefix.data(), prefix.size() * sizeof(int32_t));
+  *num_groups = (int32_t)prefix.size();
   return RX_OK;
 }
 

@@ -26,7 +26,9 @@ EXPORTED = [
     "rx_decode_attn", "rx_decode_attn_noalloc", "rx_read_status", "rx_radix_create", "rx_radix_destroy",
     "rx_radix_insert", "rx_radix_match", "rx_radix_stats", "rx_radix_acquire", "rx_radix_release",
     "rx_radix_evict", "rx_slot_pool_create", "rx_slot_pool_destroy", "rx_slot_pool_free_count",
-    "rx_slot_pool_alloc", "rx_slot_pool_release", "rx_saved_tokens", "rx_token_saving",
+    "rx_slot_pool_alloc", "rx_slot_pool_release", "rx_dfs_order", "rx_gain_groups",
+    "rx_saved_tokens",
+    "rx_token_saving",
     "rx_compute_reduction",
 ]
 
@@ -94,6 +96,8 @@ def lib():
         "rx_slot_pool_free_count": (C.c_int64, [_P]),
         "rx_slot_pool_alloc": (C.c_int, [_P, _P, C.c_int64, _I32P]),
         "rx_slot_pool_release": (C.c_int, [_P, _I32P, C.c_int64]),
+        "rx_dfs_order": (C.c_int, [_I32P, _I64P, C.c_int32, _I32P]),
+        "rx_gain_groups": (C.c_int, [_I32P, _I64P, C.c_int32, _I32P, _I32P, _I32P]),
         "rx_saved_tokens": (C.c_int64, [C.c_int64, C.c_int32]),
         "rx_token_saving": (C.c_double, [C.c_int64, C.c_int64]),
         "rx_compute_reduction": (C.c_double, [C.c_int64, C.c_int64]),
@@ -354,6 +358,33 @@ class SlotPool:
     def release(self, slots):
         s, sp = _host_i32(slots)
         _check(lib().rx_slot_pool_release(self._h, sp, int(s.shape[0])))
+
+
+def dfs_order(sequences) -> np.ndarray:
+    """rx_dfs_order: the depth-first order of the batch's radix tree (a permutation)."""
+    seqs = [np.asarray(q, np.int32) for q in sequences]
+    offs = np.zeros(len(seqs) + 1, np.int64)
+    offs[1:] = np.cumsum([len(q) for q in seqs])
+    toks = np.ascontiguousarray(np.concatenate(seqs) if seqs else np.zeros(1, np.int32))
+    order = np.zeros(max(1, len(seqs)), np.int32)
+    _check(lib().rx_dfs_order(toks.ctypes.data_as(_I32P), offs.ctypes.data_as(_I64P), len(seqs),
+                              order.ctypes.data_as(_I32P)))
+    return order[:len(seqs)].copy()
+
+
+def gain_groups(sequences):
+    """rx_gain_groups: (group_of_req, group_prefix_len) under BatchLLM's gain rule."""
+    seqs = [np.asarray(q, np.int32) for q in sequences]
+    offs = np.zeros(len(seqs) + 1, np.int64)
+    offs[1:] = np.cumsum([len(q) for q in seqs])
+    toks = np.ascontiguousarray(np.concatenate(seqs) if seqs else np.zeros(1, np.int32))
+    grp = np.zeros(max(1, len(seqs)), np.int32)
+    gpl = np.zeros(max(1, len(seqs)), np.int32)
+    ng = np.zeros(1, np.int32)
+    _check(lib().rx_gain_groups(toks.ctypes.data_as(_I32P), offs.ctypes.data_as(_I64P), len(seqs),
+                                grp.ctypes.data_as(_I32P), gpl.ctypes.data_as(_I32P),
+                                ng.ctypes.data_as(_I32P)))
+    return grp[:len(seqs)].copy(), gpl[:int(ng[0])].copy()
 
 
 def saved_tokens(matched: int, unit: int) -> int:
