@@ -111,25 +111,30 @@ class Workload:
 
 
 class Builder:
-    """Allocates runs in a randomly permuted page-1 pool and assembles req_to_token rows."""
+    """Allocates runs in a randomly permuted pool and assembles req_to_token rows.  page = 1: every
+    token a random slot; page > 1: a run takes whole pages (slots page * P + i) drawn in a random
+    page order, its last page possibly part-filled (block-granular pools)."""
 
     def __init__(self, rng: np.random.Generator, num_q_heads: int, num_kv_heads: int,
-                 pool_size: int, head_dim: int = HEAD_DIM):
+                 pool_size: int, head_dim: int = HEAD_DIM, page: int = 1):
         self.rng = rng
         self.hq, self.hkv, self.d = num_q_heads, num_kv_heads, head_dim
         self.pool_size = pool_size
-        self.perm = rng.permutation(pool_size).astype(np.int32)
+        self.page = page
+        self.perm = rng.permutation(pool_size // page).astype(np.int32)
         self.next = 0
         self.k_pool = np.zeros((pool_size, num_kv_heads, head_dim), dtype=np.uint16)
         self.v_pool = np.zeros((pool_size, num_kv_heads, head_dim), dtype=np.uint16)
         self.rows: List[np.ndarray] = []
 
     def _alloc(self, n: int) -> np.ndarray:
-        if self.next + n > self.pool_size:
+        P = self.page
+        pages = (n + P - 1) // P
+        if self.next + pages > self.perm.shape[0]:
             raise ValueError(f"pool of {self.pool_size} slots exhausted")
-        s = self.perm[self.next:self.next + n].copy()
-        self.next += n
-        return s
+        first = self.perm[self.next:self.next + pages].astype(np.int64)
+        self.next += pages
+        return (first[:, None] * P + np.arange(P)[None, :]).reshape(-1)[:n].astype(np.int32)
 
     def cached(self, n: int) -> Run:
         slots = self._alloc(n)
@@ -301,6 +306,47 @@ def decode_workload(seed: int, num_q_heads: int, num_kv_heads: int, *, n_groups:
               f"{members} requests on a cached {prefix}-token prefix; distinct U[{dist_lo},{dist_hi}]"
               f" incl. the current token; {ungrouped} ungrouped; pool {P} slots, random permutation")
     return b.finish(name, [(new_runs, None, (rows, sl, grp, gpl))], cached_seqs, recipe)
+
+
+def paged_workload(seed: int, num_q_heads: int, num_kv_heads: int, *, page: int, prefix: int,
+                   n_req: int, ext_lo: int, ext_hi: int, name: str = "paged") -> Workload:
+    """Block-granular pool (prefix-caching comparison page: vLLM keeps KV in blocks and reuses only
+    whole blocks).  n_req requests share a cached `prefix` of which only floor(prefix / page) *
+    page tokens -- whole pages -- are reused; each request recomputes the rest of the prefix and
+    its U[ext_lo, ext_hi] new tokens in pages of its own (one extend step), then decodes one token
+    (a second step)."""
+    rng = np.random.default_rng(seed)
+    shared = prefix // page * page
+    ext = rng.integers(ext_lo, ext_hi + 1, size=n_req)
+    need_pages = shared // page + int(sum((prefix - shared + e + 1 + page - 1) // page + 1 for e in ext))
+    P = max(4096, 1 << int(np.ceil(np.log2(need_pages * page * 1.25))))
+    b = Builder(rng, num_q_heads, num_kv_heads, P, page=page)
+    pre = b.cached(shared) if shared > 0 else None
+    cached_seqs = [(pre.tokens.copy(), pre.slots.copy())] if pre is not None else []
+    new_runs, rows, pl, el, toks, cur_runs = [], [], [], [], [], []
+    for i in range(n_req):
+        nr = b.new(prefix - shared + int(ext[i]))
+        new_runs.append(nr)
+        runs = ([pre] if pre is not None else []) + [nr]
+        rows.append(b.row(runs))
+        pl.append(shared)
+        el.append(int(len(nr)))
+        toks.append(_tokens(runs))
+    d_rows, d_sl, d_runs = [], [], []
+    for i in range(n_req):
+        cur = b.new(1)
+        d_runs.append(cur)
+        runs = ([pre] if pre is not None else []) + [new_runs[i], cur]
+        d_rows.append(b.row(runs))
+        d_sl.append(shared + len(new_runs[i]) + 1)
+    grp = [0 if shared > 0 else -1] * n_req
+    steps = [(new_runs, (rows, pl, el, grp, [shared], toks), None),
+             (d_runs, None, (d_rows, d_sl, grp, [shared]))]
+    recipe = (f"seed {seed}; Hq={num_q_heads} Hkv={num_kv_heads} d=128; pages of {page} slots in "
+              f"random page order; {n_req} requests on a {prefix}-token prefix of which {shared} "
+              f"(whole pages) are reused; extend U[{ext_lo},{ext_hi}] new tokens, then one decode "
+              f"step; pool {P} slots")
+    return b.finish(name, steps, cached_seqs, recipe)
 
 
 def tree_workload(seed: int, num_q_heads: int, num_kv_heads: int, *, depth: int, fanout: int,

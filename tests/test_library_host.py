@@ -224,3 +224,17 @@ def test_radix_mixed_tree_plans(librx):
     assert reads[1][0] > 2 * reads[0][0]
     # extend: branch-level packing walks fewer keys than packing at the system prompt
     assert reads[0][1] < reads[1][1]
+
+
+def test_block_granular_match_reuses_whole_pages(librx):
+    from prefix_shared_kv_gb300 import workloads as W
+    wl = W.paged_workload(77, 8, 2, page=16, prefix=1000, n_req=3, ext_lo=5, ext_hi=9)
+    tokens, slots = wl.cached_sequences[0]
+    assert len(tokens) == 992                      # 62 whole pages of the 1000-token prefix
+    t = rx.Radix()
+    t.insert(tokens, slots)
+    e = wl.steps[0].extend
+    for r in range(3):
+        saved, got = t.match(e.tokens[r], match_unit=16)
+        assert saved == 992 and np.array_equal(got, slots)
+        assert np.all(got.reshape(-1, 16) // 16 == (got.reshape(-1, 16) // 16)[:, :1])  # pages

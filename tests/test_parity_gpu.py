@@ -236,6 +236,19 @@ def test_tree_and_one_level_plans_agree(cuda):
 
 
 # ---------------------------------------------------------------------------------------------
+# Block-granular pools (prefix-caching comparison page: vLLM's 16-token blocks): the kernels index
+# KV per token slot, so a paged pool is slots page * 16 + i; only whole pages of the prefix are
+# reused and the rest is recomputed as part of the extend.
+# ---------------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("hq,hkv,prefix", [(8, 2, 1000), (32, 32, 517), (16, 16, 16)])
+def test_block_granular_pool(cuda, hq, hkv, prefix):
+    wl = W.paged_workload(40 + prefix, hq, hkv, page=16, prefix=prefix, n_req=5, ext_lo=1,
+                          ext_hi=140)
+    run_and_check(wl, cuda)
+
+
+# ---------------------------------------------------------------------------------------------
 # Full-size workloads in the benchmark's configuration, sampled requests.
 # ---------------------------------------------------------------------------------------------
 
