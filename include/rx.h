@@ -211,6 +211,13 @@ rx_status rx_decode_attn_noalloc(const rx_plan* plan, const rx_kv_desc* desc, co
  * was uploaded to.  *status receives RX_OK or the first device-side error recorded. */
 rx_status rx_read_status(const void* workspace, int32_t* status, rx_stream_t stream);
 
+/* Self-test of device-side failure detection (no counterpart on the pages).  Launches one CTA
+ * that waits, with the bounded wait every tensor-core kernel uses, for an mbarrier phase that
+ * nothing completes, giving up after limit_ns (0 < limit_ns <= 2 s); the wait then records
+ * RX_ERR_TIMEOUT in *status (device, int32, first error wins: clear it to 0 first).  The GPU and
+ * the context stay usable.  For tests of the timeout path. */
+rx_status rx_selftest_wait_timeout(int32_t* status, int64_t limit_ns, rx_stream_t stream);
+
 /* ---------------------------------------------------------------------------------------------
  * Host radix cache: token sequences -> pool slots, edges labelled with token runs (SGLang
  * explainer, RadixAttention: radix tree whose nodes refer to the pages of their tokens).

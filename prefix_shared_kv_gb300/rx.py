@@ -23,7 +23,7 @@ EXPORTED = [
     "rx_status_string", "rx_last_error", "rx_store_kv", "rx_plan_create", "rx_plan_destroy",
     "rx_plan_workspace_size", "rx_plan_upload", "rx_plan_key_reads", "rx_extend_plan",
     "rx_extend_plan_tree", "rx_extend_attn", "rx_decode_plan", "rx_decode_plan_tree",
-    "rx_decode_attn", "rx_decode_attn_noalloc", "rx_read_status", "rx_radix_create", "rx_radix_destroy",
+    "rx_decode_attn", "rx_decode_attn_noalloc", "rx_read_status", "rx_selftest_wait_timeout", "rx_radix_create", "rx_radix_destroy",
     "rx_radix_insert", "rx_radix_match", "rx_radix_stats", "rx_radix_acquire", "rx_radix_release",
     "rx_radix_evict", "rx_slot_pool_create", "rx_slot_pool_destroy", "rx_slot_pool_free_count",
     "rx_slot_pool_alloc", "rx_slot_pool_release", "rx_dfs_order", "rx_gain_groups",
@@ -83,6 +83,7 @@ def lib():
                                      _P]),
         "rx_decode_attn_noalloc": (C.c_int, [_P, C.POINTER(KVDesc), _P, _P, _P, _P, _P, _P]),
         "rx_read_status": (C.c_int, [_P, _I32P, _P]),
+        "rx_selftest_wait_timeout": (C.c_int, [_P, C.c_int64, _P]),
         "rx_radix_create": (C.c_int, [C.POINTER(_P)]),
         "rx_radix_destroy": (None, [_P]),
         "rx_radix_insert": (C.c_int, [_P, _I32P, _I32P, C.c_int64, _I64P]),
@@ -385,6 +386,11 @@ def gain_groups(sequences):
                                 grp.ctypes.data_as(_I32P), gpl.ctypes.data_as(_I32P),
                                 ng.ctypes.data_as(_I32P)))
     return grp[:len(seqs)].copy(), gpl[:int(ng[0])].copy()
+
+
+def selftest_wait_timeout(status, limit_ns: int, stream=None):
+    """rx_selftest_wait_timeout: a bounded wait that runs out; writes RX_ERR_TIMEOUT to `status`."""
+    _check(lib().rx_selftest_wait_timeout(_ptr(status), int(limit_ns), _stream(stream)))
 
 
 def saved_tokens(matched: int, unit: int) -> int:

@@ -257,3 +257,24 @@ def test_block_granular_pool(cuda, hq, hkv, prefix):
 def test_full_size_workloads_sampled(cuda, name):
     wl = W.NAMED[name]()
     run_and_check(wl, cuda, sample=6, seed=1)
+
+
+# ---------------------------------------------------------------------------------------------
+# Failure detection on the GPU without a fault: a bounded wait that nothing completes gives up,
+# records RX_ERR_TIMEOUT in the status word and leaves the context usable.
+# ---------------------------------------------------------------------------------------------
+
+def test_bounded_wait_times_out_and_the_context_stays_usable(cuda):
+    import time
+    status = torch.zeros(1, dtype=torch.int32, device=cuda)
+    t0 = time.perf_counter()
+    rx.selftest_wait_timeout(status, 20_000_000)        # 20 ms
+    torch.cuda.synchronize()
+    waited = time.perf_counter() - t0
+    assert status.item() == rx.RX_ERR_TIMEOUT
+    assert 0.015 < waited < 1.5
+    status.zero_()
+    rx.selftest_wait_timeout(status, 5_000_000)
+    torch.cuda.synchronize()
+    assert status.item() == rx.RX_ERR_TIMEOUT
+    run_and_check(W.tiny(), cuda)                        # kernels still run and agree
