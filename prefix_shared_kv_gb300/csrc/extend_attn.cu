@@ -9,8 +9,9 @@
 // keys (visible to that member's rows only, causal on its new tokens).  One online softmax runs
 // across all segments, so no partial results leave the CTA.
 //
-// Blackwell tile loop (one CTA per work item = two 128-row tiles A and B of one KV head, 512
-// threads, warp-specialised, 64 keys per step; every K/V step feeds both tiles, i.e. 256 rows):
+// Blackwell tile loop (a persistent CTA per SM walks its share of the work items; an item is two
+// 128-row tiles A and B of one KV head; 512 threads, warp-specialised, 64 keys per step; every K/V
+// step feeds both tiles, i.e. 256 rows):
 //   warps 8-10  K producers (steps t = 0, 1, 2 mod 3), warps 11-13 V producers: gather the keys'
 //              256-byte rows by slot with TMA (cp.async.bulk.tensor tile::gather4: four pool rows
 //              per instruction, 128-byte swizzle applied by the copy engine) into 5-stage rings
@@ -29,7 +30,12 @@
 //              O in TMEM rescaled -- when it grows by more than 2^8), P = exp2(.) packed to bf16
 //              and written to TMEM with tcgen05.st for the PV MMA; finally O / l and the LSE.  The
 //              two tiles take turns for the exponentials, so each has the SM's exp units to
-//              itself while the tensor core works on the other tile.
+//              itself while the tensor core works on the other tile; everything before the
+//              exponentials (loads, masks, maximum, scale-and-shift) runs outside the turn.
+// Items follow one another without a break in the pipelines: the rings, S buffers and barrier
+// phases run on across items, the query rows of the next item are copied in as soon as the last
+// S of the current one is computed, and the first two S of the next item are computed while the
+// softmax warps write out the current one.
 // Every mbarrier wait is bounded (globaltimer); a timeout records RX_ERR_TIMEOUT in the
 // workspace status word and every role leaves its loop.
 #include <cuda.h>
@@ -62,9 +68,11 @@ struct ExtParams {
   int32_t oob_row;  // a row index past the end of the pool's [pool_size * Hkv, 128] view
   float* part_o;    // non-null: write fp32 partial rows (decode shared-prefix units)
   float* part_lse;
+  int n_items;
+  bool o32;         // o is 32-byte aligned: rows go out in 32-byte stores, else 16-byte ones
 };
 
-constexpr int kN = 64;                 // keys per step
+constexpr int kN = kAttnKeys;          // keys per step (64)
 constexpr int kPW = 3;                 // producer warps per operand (one gather in issue each)
 constexpr int kWarpK = 8, kWarpV = kWarpK + kPW, kWarpMma = kWarpV + kPW;
 constexpr int kThreads = 32 * (kWarpMma + 2);  // softmax A, B | K producers | V producers | MMA A, B
@@ -97,10 +105,15 @@ constexpr int kOffBar = kOffV + kStages * kKVTile;
 //              barrier per buffer: with S_x(t+1) already computed, the softmax can finish step
 //              t+1 before the issuer has taken step t, so a single barrier could run two phases
 //              ahead of the issuer; P_x(t+2) waits for S_x(t+2), which waits for P_x(t).
-//   O_DONE[x]  every MMA of tile x complete: O_x final for the epilogue, TMEM free to release
-//   Q_FULL     both query tiles in shared memory (256 softmax threads)
+//   O_DONE[x]  every MMA of tile x's item complete: O_x final for the epilogue
+//   Q_FULL[x]  tile x's query rows in shared memory (tile x's 128 softmax threads)
 //   TURN[x]    tile x's softmax may run its exponentials for the next step (128 arrivals of the
 //              other tile's softmax): A(0), B(0), A(1), B(1), ...
+//   DRAIN[x]   every MMA of issuer x complete, at the end: TMEM may be released
+// Phases count on across items.  Per item of tile x the issuer commits S_FULL[x] for steps
+// 0 .. ntiles + 1 (the last two without an MMA), so the S steps of successive items are
+// contiguous.  In an item with tile A only, issuer B releases each ring stage with a plain
+// arrival once the stage has landed.
 enum {
   B_K_FULL = 0,
   B_K_FREE = B_K_FULL + kStages,
@@ -110,8 +123,9 @@ enum {
   B_P_FULL = B_S_FULL + 4,  // [x][b] at B_P_FULL + 2 * x + b
   B_O_DONE = B_P_FULL + 4,
   B_Q_FULL = B_O_DONE + 2,
-  B_TURN = B_Q_FULL + 1,
-  B_COUNT = B_TURN + 2
+  B_TURN = B_Q_FULL + 2,
+  B_DRAIN = B_TURN + 2,
+  B_COUNT = B_DRAIN + 2
 };
 constexpr int kOffTmem = kOffBar + B_COUNT * 8;
 constexpr int kOffAbort = kOffTmem + 8;
@@ -136,6 +150,15 @@ __device__ __forceinline__ void tile_next(TileIter& c, const ExtSeg* segs, int n
     ++c.seg;
     if (c.seg < n_seg) c.k0 = segs[c.seg].k_begin;
   }
+}
+
+// The CTA's r-th item: the plan's list is dealt to the grid in snake order (round r holds items
+// r G .. r G + G - 1; CTA k takes the k-th of an even round and the (G - 1 - k)-th of an odd one),
+// so that a list sorted by falling cost gives every CTA a similar total.  -1 past the end.
+__device__ __forceinline__ int item_at(int r, int n_items) {
+  const int G = gridDim.x, k = blockIdx.x;
+  const int64_t i = (int64_t)r * G + ((r & 1) ? G - 1 - k : k);
+  return i < n_items ? (int)i : -1;
 }
 
 // Byte offset of 16-byte chunk c (0..15) of row r in a K-major tile stored as two 128-byte-
@@ -190,54 +213,66 @@ struct Slot4 {
   int v[4];
 };
 
-__device__ __forceinline__ void producer(const ExtParams& p, const ExtItem& it,
-                                         const ExtSeg* segs, int ntiles, int w, uint32_t base,
+__device__ __forceinline__ void producer(const ExtParams& p, int w, uint32_t base,
                                          const CUtensorMap* map, uint32_t ring, int b_full,
                                          int b_free, volatile int* abort) {
   const int lane = threadIdx.x & 31;
   const int g = lane & 15, h = lane >> 4;
   const uint32_t bar = base + kOffBar;
-  TileIter at{0, segs[0].k_begin};
-  int at_step = 0;
-  auto fetch = [&](Slot4& sl, int t) {  // entries of step t (t only grows)
-    for (; at_step < t; ++at_step) tile_next(at, segs, it.n_seg);
-    const ExtSeg& sg = segs[at.seg];
+  uint32_t gs = 0;  // ring steps of the CTA's earlier items
+  for (int ri = 0;; ++ri) {
+    const int idx = item_at(ri, p.n_items);
+    if (idx < 0) return;
+    const ExtItem it = p.items[idx];
+    const ExtSeg* segs = p.segs + it.seg_begin;
+    const int ntiles = it.n_steps;
+    TileIter at{0, ntiles > 0 ? segs[0].k_begin : 0};
+    int at_step = 0;
+    auto fetch = [&](Slot4& sl, int t) {  // entries of step t (t only grows)
+      for (; at_step < t; ++at_step) tile_next(at, segs, it.n_seg);
+      const ExtSeg& sg = segs[at.seg];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) sl.v[i] = fetch_slot(p, sg, at.k0, 4 * g + i);
-  };
-  Slot4 nxt{{-1, -1, -1, -1}};
-  if (w < ntiles) fetch(nxt, w);
-  // per step: take the prefetched entries, prefetch t + kPW, wait for the stage, gather t
-  for (int t = w; t < ntiles; t += kPW) {
-    const Slot4 cur = nxt;
-    if (t + kPW < ntiles) fetch(nxt, t + kPW);
-    const int st = t % kStages;
-    const bool waited = t < kStages || tc::mbar_wait(bar + 8 * (b_free + st),
-                                                     (t / kStages - 1) & 1, abort, p.status,
-                                                     kWaitNs);
-    if (__any_sync(0xffffffffu, !waited)) break;  // the warp leaves together
-    int r[4];
+      for (int i = 0; i < 4; ++i) sl.v[i] = fetch_slot(p, sg, at.k0, 4 * g + i);
+    };
+    // this warp's steps are the ring steps w, w + kPW, ... counted over all the CTA's items
+    const int t0 = (int)((w + kPW - gs % kPW) % kPW);
+    Slot4 nxt{{-1, -1, -1, -1}};
+    if (t0 < ntiles) fetch(nxt, t0);
+    // per step: take the prefetched entries, prefetch t + kPW, wait for the stage, gather t
+    for (int t = t0; t < ntiles; t += kPW) {
+      const Slot4 cur = nxt;
+      if (t + kPW < ntiles) fetch(nxt, t + kPW);
+      const uint32_t gt = gs + t;
+      const int st = gt % kStages;
+      const bool waited = gt < kStages || tc::mbar_wait(bar + 8 * (b_free + st),
+                                                        (gt / kStages - 1) & 1, abort, p.status,
+                                                        kWaitNs);
+      if (__any_sync(0xffffffffu, !waited)) return;  // the warp leaves together
+      int r[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int v = check_slot(p, cur.v[i]);
-      r[i] = v >= 0 ? v * p.hkv + it.kv_head : p.oob_row;
+      for (int i = 0; i < 4; ++i) {
+        const int v = check_slot(p, cur.v[i]);
+        r[i] = v >= 0 ? v * p.hkv + it.kv_head : p.oob_row;
+      }
+      if (lane == 0) mbar_expect_tx(bar + 8 * (b_full + st), kN * kHeadDim * 2);
+      __syncwarp();
+      tma_gather4(ring + st * kKVTile + h * kKVHalf + g * 512, map, 64 * h, r[0], r[1], r[2],
+                  r[3], bar + 8 * (b_full + st));
     }
-    if (lane == 0) mbar_expect_tx(bar + 8 * (b_full + st), kN * kHeadDim * 2);
-    __syncwarp();
-    tma_gather4(ring + st * kKVTile + h * kKVHalf + g * 512, map, 64 * h, r[0], r[1], r[2], r[3],
-                bar + 8 * (b_full + st));
+    gs += ntiles;
   }
 }
 
-// MMA issuer of tile x (one thread): S_x(0) and S_x(1); then per step t, once P_x(t) is in
-// TMEM, PV_x(t) and S_x(t+2) right behind it (into the buffer P_x(t) sat in).  The two tiles have
-// an issuer each (the last two warps, on different SM sub-partitions); both commit to the ring
-// stages' free barriers, which therefore take two arrivals.  The MMAs of a step are issued back
-// to back and their commits follow them: a commit holds up the issuing thread's next barrier
-// operation until the tensor pipe has taken the MMAs before it, so every wait comes first.
-__device__ __forceinline__ void mma_issuer(const ExtParams& p, int x, int ntiles, uint32_t base,
+// MMA issuer of tile x (one thread), per item: S_x(0) and S_x(1); then per step t, once P_x(t) is
+// in TMEM, PV_x(t) and S_x(t+2) right behind it (into the buffer P_x(t) sat in).  The two tiles
+// have an issuer each (the last two warps, on different SM sub-partitions); both commit to the
+// ring stages' free barriers, which therefore take two arrivals.  The MMAs of a step are issued
+// back to back and their commits follow them: a commit holds up the issuing thread's next
+// barrier operation until the tensor pipe has taken the MMAs before it, so every wait comes first.
+// The S_x(0), S_x(1) of the next item go in right after PV_x of the current one's last step: the
+// tensor pipe keeps one thread's MMAs in order, so they overwrite S buffers whose P has been used.
+__device__ __forceinline__ void mma_issuer(const ExtParams& p, int x, uint32_t base,
                                            uint32_t tmem, volatile int* abort) {
-  if (ntiles < 0) return;  // no tile x in this item
   constexpr uint32_t idS = tc::idesc_bf16(128, kN, false, false);
   constexpr uint32_t idO = tc::idesc_bf16(128, 128, false, true);
   const uint32_t bar = base + kOffBar;
@@ -247,55 +282,87 @@ __device__ __forceinline__ void mma_issuer(const ExtParams& p, int x, int ntiles
   const uint64_t kdesc0 = tc::desc_sw128(base + kOffK, 16, 1024);
   const uint64_t vdesc0 = tc::desc_sw128(base + kOffV, kKVHalf, 1024);
   const uint32_t d_o = tmem + kColO + x * 128;
-  bool ok = true, issued = false;
+  bool ok = true;
   auto wait = [&](int b, uint32_t parity) {
     ok = ok && tc::mbar_wait(bar + 8 * b, parity, abort, p.status, kWaitNs);
     return ok;
   };
-  auto qk = [&](int t) {  // S_x(t) = Q_x K(t)^T into buffer t % 2
-    const uint64_t kd = kdesc0 + (((t % kStages) * kKVTile) >> 4);
-    const uint32_t d_s = tmem + col_s_of(x, t & 1);
-#pragma unroll
-    for (int s = 0; s < 8; ++s)
-      tc::mma_ss(d_s, qdesc + (((s >> 2) * kQHalf + (s & 3) * 32) >> 4),
-                 kd + (((s >> 2) * kKVHalf + (s & 3) * 32) >> 4), idS, s > 0 ? 1u : 0u);
-    issued = true;
-  };
-  auto pv = [&](int t) {  // O_x += P_x(t) V(t)
-    const uint64_t vd = vdesc0 + (((t % kStages) * kKVTile) >> 4);
-    const uint32_t a_p = tmem + col_s_of(x, t & 1) + kPOff;
-#pragma unroll
-    for (int s = 0; s < kN / 16; ++s)
-      tc::mma_ts(d_o, a_p + 8 * s, vd + ((s * 2048) >> 4), idO, (t > 0 || s > 0) ? 1u : 0u);
-  };
-  if (ntiles > 0 && wait(B_Q_FULL, 0)) {
-    for (int t = 0; t < 2 && t < ntiles; ++t) {
-      if (!wait(B_K_FULL + t, 0)) break;
-      tc::fence_after();
-      qk(t);
-      tc::commit(bar + 8 * (B_S_FULL + 2 * x + t));
-      tc::commit(bar + 8 * (B_K_FREE + t));
+  // running counts over the CTA's earlier items: ring steps, S steps of tile x (ntiles + 2 per
+  // item), P steps of tile x, items of tile x
+  uint32_t gs = 0, sv = 0, pb = 0, nq = 0;
+  for (int ri = 0; ok; ++ri) {
+    const int idx = item_at(ri, p.n_items);
+    if (idx < 0) break;
+    const ExtItem it = p.items[idx];
+    const int ntiles = it.n_steps;
+    const bool two = it.n_tok[1] > 0;
+    if (ntiles == 0) continue;  // (plans hold none; every role skips them alike)
+    if (x == 1 && !two) {
+      // no tile B: release the item's ring stages beside issuer A, one step after another (so
+      // this thread never tests a ring barrier two phases away from the one it waits for)
+      for (int t = 0; t < ntiles; ++t) {
+        const uint32_t gt = gs + t;
+        if (!wait(B_K_FULL + gt % kStages, (gt / kStages) & 1)) break;
+        tc::mbar_arrive(bar + 8 * (B_K_FREE + gt % kStages));
+        if (!wait(B_V_FULL + gt % kStages, (gt / kStages) & 1)) break;
+        tc::mbar_arrive(bar + 8 * (B_V_FREE + gt % kStages));
+      }
+      gs += ntiles;
+      continue;
     }
-  }
-  for (int t = 0; ok && t < ntiles; ++t) {
-    const int t2 = t + 2;
-    const bool more = t2 < ntiles;
-    if (!wait(B_P_FULL + 2 * x + (t & 1), (t >> 1) & 1) ||
-        !wait(B_V_FULL + t % kStages, (t / kStages) & 1) ||
-        (more && !wait(B_K_FULL + t2 % kStages, (t2 / kStages) & 1)))
-      break;
-    tc::fence_after();
-    pv(t);
-    if (more) qk(t2);
-    tc::commit(bar + 8 * (B_V_FREE + t % kStages));
-    tc::commit(bar + 8 * (B_S_FULL + 2 * x + (t & 1)));  // also after the last steps: see above
-    if (more) tc::commit(bar + 8 * (B_K_FREE + t2 % kStages));
-  }
-  // every MMA issued above completes before O is read out and TMEM is released
-  if (issued) {
+    auto release = [&](int b, uint32_t gt) { tc::commit(bar + 8 * (b + (int)(gt % kStages))); };
+    auto qk = [&](int t) {  // S_x(t) = Q_x K(t)^T into buffer (sv + t) % 2
+      const uint64_t kd = kdesc0 + ((((gs + t) % kStages) * kKVTile) >> 4);
+      const uint32_t d_s = tmem + col_s_of(x, (sv + t) & 1);
+#pragma unroll
+      for (int s = 0; s < 8; ++s)
+        tc::mma_ss(d_s, qdesc + (((s >> 2) * kQHalf + (s & 3) * 32) >> 4),
+                   kd + (((s >> 2) * kKVHalf + (s & 3) * 32) >> 4), idS, s > 0 ? 1u : 0u);
+    };
+    auto pv = [&](int t) {  // O_x += P_x(t) V(t)
+      const uint64_t vd = vdesc0 + ((((gs + t) % kStages) * kKVTile) >> 4);
+      const uint32_t a_p = tmem + col_s_of(x, (sv + t) & 1) + kPOff;
+#pragma unroll
+      for (int s = 0; s < kN / 16; ++s)
+        tc::mma_ts(d_o, a_p + 8 * s, vd + ((s * 2048) >> 4), idO, (t > 0 || s > 0) ? 1u : 0u);
+    };
+    if (!wait(B_Q_FULL + x, nq & 1)) break;
+    for (int t = 0; t < 2; ++t) {
+      if (t < ntiles) {
+        if (!wait(B_K_FULL + (gs + t) % kStages, ((gs + t) / kStages) & 1)) break;
+        tc::fence_after();
+        qk(t);
+        tc::commit(bar + 8 * (B_S_FULL + 2 * x + ((sv + t) & 1)));
+        release(B_K_FREE, gs + t);
+      } else {
+        tc::commit(bar + 8 * (B_S_FULL + 2 * x + ((sv + t) & 1)));  // step without an MMA
+      }
+    }
+    for (int t = 0; ok && t < ntiles; ++t) {
+      const uint32_t gt = gs + t, gt2 = gt + 2;
+      const bool more = t + 2 < ntiles;
+      if (!wait(B_P_FULL + 2 * x + ((pb + t) & 1), ((pb + t) >> 1) & 1) ||
+          !wait(B_V_FULL + gt % kStages, (gt / kStages) & 1) ||
+          (more && !wait(B_K_FULL + gt2 % kStages, (gt2 / kStages) & 1)))
+        break;
+      tc::fence_after();
+      pv(t);
+      if (more) qk(t + 2);
+      release(B_V_FREE, gt);
+      tc::commit(bar + 8 * (B_S_FULL + 2 * x + ((sv + t) & 1)));  // also after the last steps
+      if (more) release(B_K_FREE, gt2);
+    }
+    if (!ok) break;
     tc::commit(bar + 8 * (B_O_DONE + x));
-    tc::mbar_wait(bar + 8 * (B_O_DONE + x), 0, abort, p.status, kWaitNs);
+    gs += ntiles;
+    sv += ntiles + 2;
+    pb += ntiles;
+    ++nq;
   }
+  // every MMA issued above completes before TMEM is released, after an abort too
+  tc::commit(bar + 8 * (B_DRAIN + x));
+  int no_abort = 0;
+  tc::mbar_wait(bar + 8 * (B_DRAIN + x), 0, &no_abort, p.status, kWaitNs);
 }
 
 // Row maximum of the 64 raw scores (three-input maxima, eight independent chains).  Masked keys
@@ -317,12 +384,10 @@ __device__ __forceinline__ float row_max(const uint32_t (&sr)[2][32]) {
   return fmax3(m[0], m[1], fmaxf(m[6], m[7]));
 }
 
-// p_j = 2^(s_j * scale_log2 - m), packed to bf16 pairs in pk (a masked key's -inf gives 0); returns
-// the sum of the p_j.  The scale-and-shift and the sums run on packed fp32 pairs.  m is finite.
-__device__ __forceinline__ float row_exp(const uint32_t (&sr)[2][32], float sl2, float m,
-                                         uint32_t (&pk)[32]) {
+// In place, on packed fp32 pairs: s_j -> s_j * scale_log2 - m (a masked key's -inf stays -inf; m
+// is finite).
+__device__ __forceinline__ void row_shift(uint32_t (&sr)[2][32], float sl2, float m) {
   const uint64_t k2 = f2_pack(sl2, sl2), nm2 = f2_pack(-m, -m);
-  uint64_t acc[2] = {0ull, 0ull};  // two chains of (even, odd) partial sums
 #pragma unroll
   for (int q = 0; q < 2; ++q)
 #pragma unroll
@@ -331,80 +396,116 @@ __device__ __forceinline__ float row_exp(const uint32_t (&sr)[2][32], float sl2,
       f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[q][j]), __uint_as_float(sr[q][j + 1])), k2,
                        nm2),
                 x0, x1);
-      const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
-      acc[(j >> 1) & 1] = f2_add(acc[(j >> 1) & 1], f2_pack(p0, p1));
-      pk[16 * q + (j >> 1)] = pack_bf16(p0, p1);
+      sr[q][j] = __float_as_uint(x0);
+      sr[q][j + 1] = __float_as_uint(x1);
     }
-  float a0, a1, b0, b1;
-  f2_unpack(acc[0], a0, a1);
-  f2_unpack(acc[1], b0, b1);
-  return (a0 + a1) + (b0 + b1);
 }
 
-// TWO: tile B present, the tiles take turns for the exponentials (a compile-time choice: a runtime
-// test inside the step loop costs a few percent)
-template <bool TWO>
-__device__ __forceinline__ void softmax_rows(const ExtParams& p, const ExtItem& it,
-                                             const ExtSeg* segs, int ntiles, uint32_t base,
-                                             uint32_t tmem, volatile int* abort) {
-  constexpr bool two = TWO;
-  const int x = threadIdx.x >> 7;   // tile: 0 = A, 1 = B
-  const int r = threadIdx.x & 127;  // query row of the tile == TMEM lane
-  const int wq = (threadIdx.x >> 5) & 3;
-  const uint32_t lane_t = tmem + ((uint32_t)(32 * wq) << 16);
-  const uint32_t col_o = kColO + x * 128;
-  const uint32_t bar = base + kOffBar;
-  // (selects rather than it.n_tok[x]: indexing the item with a runtime x would put it on the stack)
-  const int n_rows = (x ? it.n_tok[1] : it.n_tok[0]) * p.gq;
-  const bool valid = r < n_rows;
-  int owner = -2, kmax = 0, q_row = 0;
-  if (valid) {
-    const ExtRow e = p.rows[(x ? it.row_begin[1] : it.row_begin[0]) + r / p.gq];
-    owner = e.owner;
-    kmax = e.kmax;
-    q_row = e.q_row;
-  }
-  const int qh = it.kv_head * p.gq + (r % p.gq);
-  {
-    // query row r -> the tile's Q buffer (16 chunks of 16 bytes), then visible to the tensor core
-    const __nv_bfloat16* src = p.q + ((int64_t)q_row * p.hq + qh) * kHeadDim;
-    const uint32_t qb = base + kOffQ + x * kQTile;
+// p_e = 2^x_e for the row's 64 elements (-inf gives 0), packed to bf16 pairs in pk and added into
+// two chains of packed (even, odd) partial sums.
+__device__ __forceinline__ void row_exp(const uint32_t (&sr)[2][32], uint32_t (&pk)[32],
+                                        uint64_t (&acc)[2]) {
 #pragma unroll
-    for (int c = 0; c < 16; ++c)
-      cp_async16(qb + tile_off(r, c, kQHalf), valid ? src + c * 8 : p.q, valid);
-    cp_async_commit();
-    cp_async_wait<0>();
-    tc::fence_proxy_async();
-    tc::mbar_arrive(bar + 8 * B_Q_FULL);
+  for (int e = 0; e < kN; e += 2) {
+    const int q = e >> 5, j = e & 31;
+    const float p0 = fast_exp2(__uint_as_float(sr[q][j]));
+    const float p1 = fast_exp2(__uint_as_float(sr[q][j + 1]));
+    acc[(j >> 1) & 1] = f2_add(acc[(j >> 1) & 1], f2_pack(p0, p1));
+    pk[e >> 1] = pack_bf16(p0, p1);
   }
+}
+
+// 32 bytes to global memory (the address 32-byte aligned).
+__device__ __forceinline__ void st_global_v8(void* dst, const uint32_t* w) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "r"(w[0]),
+               "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+               : "memory");
+}
+
+// A softmax thread's query row in an item: row r of tile x.
+struct RowQ {
+  int owner, kmax, q_row, qh;
+  bool valid;
+};
+
+__device__ __forceinline__ RowQ row_of(const ExtParams& p, const ExtItem& it, int x, int r) {
+  // (selects rather than it.n_tok[x]: indexing the item with a runtime x would put it on the stack)
+  RowQ q{-2, 0, 0, it.kv_head * p.gq + (r % p.gq), false};
+  if (r < (x ? it.n_tok[1] : it.n_tok[0]) * p.gq) {
+    const ExtRow e = p.rows[(x ? it.row_begin[1] : it.row_begin[0]) + r / p.gq];
+    q.owner = e.owner;
+    q.kmax = e.kmax;
+    q.q_row = e.q_row;
+    q.valid = true;
+  }
+  return q;
+}
+
+// Starts the copy of the thread's query row into row r of the tile's Q buffer (16 chunks of 16
+// bytes; zeros for a row past the tile's rows).
+__device__ __forceinline__ void load_q(const ExtParams& p, const RowQ& q, uint32_t qb, int r) {
+  const __nv_bfloat16* src = p.q + ((int64_t)q.q_row * p.hq + q.qh) * kHeadDim;
+#pragma unroll
+  for (int c = 0; c < 16; ++c)
+    cp_async16(qb + tile_off(r, c, kQHalf), q.valid ? src + c * 8 : p.q, q.valid);
+  cp_async_commit();
+}
+
+// Whether tile x's softmax and issuer take part in an item (items without steps: none).
+__device__ __forceinline__ bool has_tile(const ExtItem& it, int x) {
+  return it.n_steps > 0 && (x == 0 || it.n_tok[1] > 0);
+}
+
+// The CTA's first item from round *ri on that has tile x (-1: none); *ri is left at its round.
+__device__ __forceinline__ int first_item(const ExtParams& p, int x, int* ri) {
+  for (;; ++*ri) {
+    const int idx = item_at(*ri, p.n_items);
+    if (idx < 0 || has_tile(p.items[idx], x)) return idx;
+  }
+}
+
+// Running counts over the CTA's earlier items of tile x: S steps (ntiles + 2 per item), P steps,
+// exponential turns (steps of items with both tiles), items.
+struct SmCounts {
+  uint32_t sv, pb, tb, nq;
+};
+
+// The steps of one item for a softmax thread (TWO: tile B present, the tiles take turns for the
+// exponentials -- a compile-time choice: a runtime test inside the step loop costs a few percent).
+// At the first step ahead() looks up the next item's row; at the last step, once S_x of it is in
+// TMEM (every S_x of the item computed, the Q buffer no longer read), prefetch() starts the copy
+// of the next item's query row.  Returns false when a wait gave up (the warp then leaves
+// together).
+template <bool TWO, class Ahead, class Prefetch>
+__device__ __forceinline__ bool softmax_steps(const ExtParams& p, const ExtItem& it,
+                                              const ExtSeg* segs, int ntiles, const RowQ& row,
+                                              const SmCounts& c, uint32_t bar, uint32_t lane_t,
+                                              volatile int* abort, float& m_used, float& l,
+                                              Ahead&& ahead, Prefetch&& prefetch) {
+  constexpr bool two = TWO;
+  const int x = threadIdx.x >> 7;  // tile: 0 = A, 1 = B
+  const uint32_t col_o = kColO + x * 128;
   const float sl2 = p.scale_log2;
-  float m_used = -CUDART_INF_F, l = 0.f;
   TileIter cur{0, segs[0].k_begin};
-  bool ok = true;
-  if (x == 1 && ntiles > 0) tc::mbar_arrive(bar + 8 * B_TURN);  // tile A goes first
+  if (two && x == 1) tc::mbar_arrive(bar + 8 * B_TURN);  // tile A goes first
   // (a lone tile A takes no turns)
   for (int t = 0; t < ntiles; ++t) {
-    const uint32_t col_s = col_s_of(x, t & 1);
-    const bool w_ok = tc::mbar_wait(bar + 8 * (B_S_FULL + 2 * x + (t & 1)), (t >> 1) & 1, abort,
+    const uint32_t vs = c.sv + t;  // S step
+    const uint32_t col_s = col_s_of(x, vs & 1);
+    const bool w_ok = tc::mbar_wait(bar + 8 * (B_S_FULL + 2 * x + (vs & 1)), (vs >> 1) & 1, abort,
                                     p.status, kWaitNs);
-    if (__any_sync(0xffffffffu, !w_ok)) {  // the warp leaves together
-      ok = false;
-      break;
-    }
+    if (__any_sync(0xffffffffu, !w_ok)) return false;
     tc::fence_after();
+    if (t == 0) ahead();
+    if (t == ntiles - 1) prefetch();
     const ExtSeg sg = segs[cur.seg];
-    const bool vis = valid && (sg.owner < 0 || sg.owner == owner);
-    const int lim = vis ? min(kmax, sg.k_end) : 0;  // keys at positions >= lim are masked
+    const bool vis = row.valid && (sg.owner < 0 || sg.owner == row.owner);
+    const int lim = vis ? min(row.kmax, sg.k_end) : 0;  // keys at positions >= lim are masked
     const int n_ok = max(0, min(kN, lim - cur.k0));
     uint32_t sr[2][32];
     tc::ld32(lane_t + col_s, sr[0]);
     tc::ld32(lane_t + col_s + 32, sr[1]);
     tc::wait_ld();
-    const bool turn = !two || tc::mbar_wait(bar + 8 * (B_TURN + x), t & 1, abort, p.status, kWaitNs);
-    if (__any_sync(0xffffffffu, !turn)) {
-      ok = false;
-      break;
-    }
     if (n_ok < kN) {  // keys at n_ok and beyond are masked: -inf
 #pragma unroll
       for (int q = 0; q < 2; ++q)
@@ -418,20 +519,31 @@ __device__ __forceinline__ void softmax_rows(const ExtParams& p, const ExtItem& 
     const bool rescale = __any_sync(0xffffffffu, need);
     const float alpha = need ? fast_exp2(m_used - m_new) : 1.f;  // exp2(-inf) = 0
     if (need) m_used = m_new;
-    uint32_t pk[32];
     // a row that has seen no visible key yet has m_used = -inf and only masked keys: any finite
     // reference gives p = 0 for them
-    l = l * alpha + row_exp(sr, sl2, m_used == -CUDART_INF_F ? 0.f : m_used, pk);
+    row_shift(sr, sl2, m_used == -CUDART_INF_F ? 0.f : m_used);
+    // only the exponentials wait for the turn: masking, the maximum and the scale-and-shift run
+    // while the other tile has the exp units
+    const bool turn = !two || tc::mbar_wait(bar + 8 * (B_TURN + x), (c.tb + t) & 1, abort,
+                                            p.status, kWaitNs);
+    if (__any_sync(0xffffffffu, !turn)) return false;
+    uint32_t pk[32];
+    uint64_t acc[2] = {0ull, 0ull};
+    row_exp(sr, pk, acc);
     if (two && (x == 0 || t + 1 < ntiles)) tc::mbar_arrive(bar + 8 * (B_TURN + 1 - x));  // other's turn
+    {
+      float a0, a1, b0, b1;
+      f2_unpack(acc[0], a0, a1);
+      f2_unpack(acc[1], b0, b1);
+      l = l * alpha + ((a0 + a1) + (b0 + b1));
+    }
     if (rescale && t > 0) {
-      // O_x must hold PV_x(t-1): the phase of step t+1 of S_FULL covers it, and PV_x(t) waits for
-      // this step's P
-      const bool w2 = tc::mbar_wait(bar + 8 * (B_S_FULL + 2 * x + ((t + 1) & 1)),
-                                    ((t + 1) >> 1) & 1, abort, p.status, kWaitNs);
-      if (__any_sync(0xffffffffu, !w2)) {
-        ok = false;
-        break;
-      }
+      // O_x must hold PV_x(t-1): the phase of S step t+1 covers it, and PV_x(t) waits for this
+      // step's P
+      const uint32_t vn = vs + 1;
+      const bool w2 = tc::mbar_wait(bar + 8 * (B_S_FULL + 2 * x + (vn & 1)), (vn >> 1) & 1, abort,
+                                    p.status, kWaitNs);
+      if (__any_sync(0xffffffffu, !w2)) return false;
       tc::fence_after();
 #pragma unroll 1
       for (int q4 = 0; q4 < 4; ++q4) {
@@ -446,52 +558,147 @@ __device__ __forceinline__ void softmax_rows(const ExtParams& p, const ExtItem& 
     tc::st32(lane_t + col_s + kPOff, pk);
     tc::wait_st();
     tc::fence_before();
-    tc::mbar_arrive(bar + 8 * (B_P_FULL + 2 * x + (t & 1)));
+    tc::mbar_arrive(bar + 8 * (B_P_FULL + 2 * x + ((c.pb + t) & 1)));
     tile_next(cur, segs, it.n_seg);
   }
-  if (!ok || ntiles == 0) return;
-  const bool w_ok = tc::mbar_wait(bar + 8 * (B_O_DONE + x), 0, abort, p.status, kWaitNs);
-  if (__any_sync(0xffffffffu, !w_ok)) return;
-  tc::fence_after();
-  const float inv = l > 0.f ? 1.f / l : 0.f;
-  // final rows: bf16 O and natural-log LSE; decode shared-prefix units: fp32 partial rows and
-  // base-2 LSE for the merge (row part[x] + r, part re-read from the table)
+  return true;
+}
+
+// O_x / l out of TMEM: bf16 O and natural-log LSE; for decode shared-prefix units fp32 partial
+// rows and base-2 LSE for the merge (row part[x] + r of the item).
+__device__ __forceinline__ void write_rows(const ExtParams& p, int idx, const RowQ& row,
+                                           uint32_t lane_t, float m_used, float l) {
+  const int x = threadIdx.x >> 7, r = threadIdx.x & 127;
+  const uint32_t col_o = kColO + x * 128;
+  // l = 0: no key was visible: the row is zeros, whatever O_x holds
+  const bool none = !(l > 0.f);
+  const float inv = none ? 0.f : 1.f / l;
   const bool partial = p.part_o != nullptr;
   int64_t prow = 0;
   if (partial) {
-    const ExtItem& itg = p.items[blockIdx.x];
+    const ExtItem& itg = p.items[idx];
     prow = (int64_t)__ldg(x ? &itg.part[1] : &itg.part[0]) + r;
   }
-  __nv_bfloat16* dst = p.o + ((int64_t)q_row * p.hq + qh) * kHeadDim;
+  __nv_bfloat16* dst = p.o + ((int64_t)row.q_row * p.hq + row.qh) * kHeadDim;
   float* pdst = p.part_o + prow * kHeadDim;
 #pragma unroll 1
   for (int q4 = 0; q4 < 4; ++q4) {
     uint32_t ov[32];
     tc::ld32(lane_t + col_o + 32 * q4, ov);
     tc::wait_ld();
-    if (valid && partial) {
+    if (none) {
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
-        *reinterpret_cast<float4*>(pdst + 32 * q4 + 4 * j) =
-            make_float4(__uint_as_float(ov[4 * j]) * inv, __uint_as_float(ov[4 * j + 1]) * inv,
-                        __uint_as_float(ov[4 * j + 2]) * inv, __uint_as_float(ov[4 * j + 3]) * inv);
-    } else if (valid) {
+      for (int j = 0; j < 32; ++j) ov[j] = 0u;
+    }
+    // 32-byte stores where alignment allows: each thread writes a row of its own, so a store
+    // instruction touches 32 rows; wider stores mean fewer of them (partial rows sit in the
+    // 256-byte aligned workspace)
+    if (row.valid && partial) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) ov[j] = __float_as_uint(__uint_as_float(ov[j]) * inv);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) st_global_v8(pdst + 32 * q4 + 8 * j, &ov[8 * j]);
+    } else if (row.valid) {
       uint32_t w[16];
 #pragma unroll
       for (int j = 0; j < 16; ++j)
         w[j] = pack_bf16(__uint_as_float(ov[2 * j]) * inv, __uint_as_float(ov[2 * j + 1]) * inv);
+      if (p.o32) {
 #pragma unroll
-      for (int j = 0; j < 4; ++j)
-        *reinterpret_cast<uint4*>(dst + 32 * q4 + 8 * j) =
-            make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+        for (int j = 0; j < 2; ++j) st_global_v8(dst + 32 * q4 + 16 * j, &w[8 * j]);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          *reinterpret_cast<uint4*>(dst + 32 * q4 + 8 * j) =
+              make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+      }
     }
   }
-  if (!valid) return;
+  if (!row.valid) return;
   const float lse2 = l > 0.f ? m_used + __log2f(l) : -CUDART_INF_F;
   if (partial)
     p.part_lse[prow] = lse2;
   else
-    p.lse[(int64_t)q_row * p.hq + qh] = lse2 * 0.69314718055994530942f;
+    p.lse[(int64_t)row.q_row * p.hq + row.qh] = lse2 * 0.69314718055994530942f;
+}
+
+// Softmax thread r of tile x (TMEM lane r) over the CTA's items of tile x.  The next item's
+// record is loaded when an item starts and its row at the item's first step, so neither load
+// waits at the item boundary.
+__device__ __forceinline__ void softmax_role(const ExtParams& p, uint32_t base, uint32_t tmem,
+                                             volatile int* abort) {
+  const int x = threadIdx.x >> 7;
+  const int r = threadIdx.x & 127;
+  const int wq = (threadIdx.x >> 5) & 3;
+  const uint32_t lane_t = tmem + ((uint32_t)(32 * wq) << 16);
+  const uint32_t bar = base + kOffBar;
+  const uint32_t qb = base + kOffQ + x * kQTile;
+  int ri = 0;
+  int idx = first_item(p, x, &ri);
+  if (idx < 0) return;
+  ExtItem it = p.items[idx];
+  RowQ row = row_of(p, it, x, r);
+  load_q(p, row, qb, r);
+  cp_async_wait<0>();
+  tc::fence_proxy_async();
+  tc::mbar_arrive(bar + 8 * (B_Q_FULL + x));
+  SmCounts c{0u, 0u, 0u, 0u};
+  for (;;) {
+    const ExtSeg* segs = p.segs + it.seg_begin;
+    const int ntiles = it.n_steps;
+    const bool two = it.n_tok[1] > 0;
+    const int nidx = item_at(ri + 1, p.n_items);
+    ExtItem nit = it;
+    if (nidx >= 0) nit = p.items[nidx];
+    RowQ nrow = row;
+    bool pre = false;  // the next item has tile x: its query row is copied in during this one
+    auto ahead = [&]() {
+      if (nidx >= 0 && has_tile(nit, x)) {
+        nrow = row_of(p, nit, x, r);
+        pre = true;
+      }
+    };
+    auto prefetch = [&]() {
+      if (pre) load_q(p, nrow, qb, r);
+    };
+    float m_used = -CUDART_INF_F, l = 0.f;
+    const bool ok = two ? softmax_steps<true>(p, it, segs, ntiles, row, c, bar, lane_t, abort,
+                                              m_used, l, ahead, prefetch)
+                        : softmax_steps<false>(p, it, segs, ntiles, row, c, bar, lane_t, abort,
+                                               m_used, l, ahead, prefetch);
+    if (!ok) return;
+    if (pre) {  // the next item's query rows: its S_x(0), S_x(1) run during the write-out
+      cp_async_wait<0>();
+      tc::fence_proxy_async();
+      tc::mbar_arrive(bar + 8 * (B_Q_FULL + x));
+    }
+    const bool w_ok = tc::mbar_wait(bar + 8 * (B_O_DONE + x), c.nq & 1, abort, p.status, kWaitNs);
+    if (__any_sync(0xffffffffu, !w_ok)) return;
+    tc::fence_after();
+    write_rows(p, idx, row, lane_t, m_used, l);
+    c.sv += ntiles + 2;
+    c.pb += ntiles;
+    if (two) c.tb += ntiles;
+    ++c.nq;
+    ++ri;
+    if (nidx < 0) return;
+    if (pre) {
+      idx = nidx;
+      it = nit;
+      row = nrow;
+      continue;
+    }
+    // the next item is not one of tile x's (tile B, and an item with tile A only): find the next
+    // one that is and copy its query rows in now
+    idx = first_item(p, x, &ri);
+    if (idx < 0) return;
+    it = p.items[idx];
+    row = row_of(p, it, x, r);
+    load_q(p, row, qb, r);
+    cp_async_wait<0>();
+    tc::fence_proxy_async();
+    tc::mbar_arrive(bar + 8 * (B_Q_FULL + x));
+  }
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -501,18 +708,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023) & ~1023u;
   uint8_t* sp = smem_raw + (base - raw);
-  const ExtItem it = p.items[blockIdx.x];
   const int warp = threadIdx.x >> 5;
-  const ExtSeg* segs = p.segs + it.seg_begin;  // small, read through the L1 by every role
   volatile int* abort = reinterpret_cast<volatile int*>(sp + kOffAbort);
-  const bool two = it.n_tok[1] > 0;  // tile B present (else tile A runs alone)
   if (threadIdx.x == 0) {
     const uint32_t bar = base + kOffBar;
     for (int i = 0; i < kStages; ++i) {
       tc::mbar_init(bar + 8 * (B_K_FULL + i), 1);
-      tc::mbar_init(bar + 8 * (B_K_FREE + i), two ? 2 : 1);
+      tc::mbar_init(bar + 8 * (B_K_FREE + i), 2);
       tc::mbar_init(bar + 8 * (B_V_FULL + i), 1);
-      tc::mbar_init(bar + 8 * (B_V_FREE + i), two ? 2 : 1);
+      tc::mbar_init(bar + 8 * (B_V_FREE + i), 2);
     }
     for (int i = 0; i < 4; ++i) {
       tc::mbar_init(bar + 8 * (B_S_FULL + i), 1);
@@ -520,9 +724,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int x = 0; x < 2; ++x) {
       tc::mbar_init(bar + 8 * (B_O_DONE + x), 1);
+      tc::mbar_init(bar + 8 * (B_Q_FULL + x), 128);
       tc::mbar_init(bar + 8 * (B_TURN + x), 128);
+      tc::mbar_init(bar + 8 * (B_DRAIN + x), 1);
     }
-    tc::mbar_init(bar + 8 * B_Q_FULL, two ? 256 : 128);
     *abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -531,25 +736,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc::fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sp + kOffTmem);
-  int ntiles = 0;
-  for (int s = 0; s < it.n_seg; ++s) ntiles += (segs[s].k_end - segs[s].k_begin + kN - 1) / kN;
 
   if (warp < kWarpK) {
     tc::regs_inc<kRegsSoftmax>();
-    if (two)
-      softmax_rows<true>(p, it, segs, ntiles, base, tmem, abort);
-    else if (warp < 4)
-      softmax_rows<false>(p, it, segs, ntiles, base, tmem, abort);
+    softmax_role(p, base, tmem, abort);
   } else {
     tc::regs_dec<kRegsOther>();
     if (warp < kWarpMma) {
       const bool k = warp < kWarpV;
-      producer(p, it, segs, ntiles, warp - (k ? kWarpK : kWarpV), base, k ? &k_map : &v_map,
-               base + (k ? kOffK : kOffV), k ? B_K_FULL : B_V_FULL, k ? B_K_FREE : B_V_FREE,
-               abort);
+      producer(p, warp - (k ? kWarpK : kWarpV), base, k ? &k_map : &v_map,
+               base + (k ? kOffK : kOffV), k ? B_K_FULL : B_V_FULL, k ? B_K_FREE : B_V_FREE, abort);
     } else {
-      const int x = warp - kWarpMma;
-      if ((threadIdx.x & 31) == 0) mma_issuer(p, x, (x == 1 && !two) ? -1 : ntiles, base, tmem, abort);
+      if ((threadIdx.x & 31) == 0) mma_issuer(p, warp - kWarpMma, base, tmem, abort);
       __syncwarp();
     }
   }
@@ -631,7 +829,15 @@ int launch_attn_items(const rx_kv_desc* d, const ExtItem* items, const ExtRow* r
   if (!e) e = make_pool_map(&v_map, v_pool, d);
   if (e) return e;
   p.oob_row = (int32_t)(d->pool_size * d->num_kv_heads);
-  extend_tc_kernel<<<n_items, kThreads, kSmem, (cudaStream_t)stream>>>(p, k_map, v_map);
+  p.n_items = n_items;
+  p.o32 = (reinterpret_cast<uintptr_t>(o) & 31u) == 0;
+  // one persistent CTA per SM (a CTA fills an SM's shared memory), at most one per item
+  int dev = 0, n_sm = 0;
+  cudaError_t ce = cudaGetDevice(&dev);
+  if (ce == cudaSuccess) ce = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
+  if (ce != cudaSuccess) return (int)ce;
+  const int grid = n_items < n_sm ? n_items : n_sm;
+  extend_tc_kernel<<<grid, kThreads, kSmem, (cudaStream_t)stream>>>(p, k_map, v_map);
   return (int)cudaGetLastError();
 }
 

@@ -100,6 +100,11 @@ struct rx_plan {
 
 namespace {
 
+// Steps of the tensor-core attention kernel over a segment of n keys, and an item's cost in
+// units of a one-tile step (a step with both tiles takes about 7/6 of one).
+int32_t attn_steps(int64_t n) { return (int32_t)((n + kAttnKeys - 1) / kAttnKeys); }
+int64_t attn_cost(const ExtItem& it) { return (int64_t)it.n_steps * (it.n_tok[1] > 0 ? 7 : 6); }
+
 template <typename T>
 void put(std::vector<uint8_t>& blob, int64_t off, const std::vector<T>& v) {
   if (!v.empty()) std::memcpy(blob.data() + off, v.data(), v.size() * sizeof(T));
@@ -382,7 +387,7 @@ rx_status rx_decode_plan_tree(rx_plan* plan, const rx_kv_desc* desc, int32_t bat
             it.seg_begin = seg;
             it.n_seg = 1;
             it.kv_head = h;
-            it.pad = 0;
+            it.n_steps = attn_steps(c1 - c0);
             it.part[0] = (int32_t)(part[k] + (int64_t)h * tiles[k].n_tok * gq);
             it.part[1] = pair ? (int32_t)(part[k + 1] + (int64_t)h * tiles[k + 1].n_tok * gq) : 0;
             xitems.push_back(it);
@@ -437,9 +442,8 @@ rx_status rx_decode_plan_tree(rx_plan* plan, const rx_kv_desc* desc, int32_t bat
   std::stable_sort(items.begin(), items.end(),
                    [&](const DecItem& a, const DecItem& b) { return cost(a) > cost(b); });
 
-  std::stable_sort(xitems.begin(), xitems.end(), [&](const ExtItem& a, const ExtItem& b) {
-    return xsegs[a.seg_begin].k_end - xsegs[a.seg_begin].k_begin >
-           xsegs[b.seg_begin].k_end - xsegs[b.seg_begin].k_begin;
+  std::stable_sort(xitems.begin(), xitems.end(), [](const ExtItem& a, const ExtItem& b) {
+    return attn_cost(a) > attn_cost(b);
   });
 
   std::vector<int32_t> midx(batch + 1, 0);
@@ -686,9 +690,16 @@ rx_status rx_extend_plan_tree(rx_plan* plan, const rx_kv_desc* desc, int32_t bat
         it.seg_begin = pr.seg_begin;
         it.n_seg = pr.n_seg;
         it.kv_head = h;
-        it.pad = 0;
+        it.n_steps = 0;
+        for (int i = 0; i < pr.n_seg; ++i)
+          it.n_steps += attn_steps(segs[pr.seg_begin + i].k_end - segs[pr.seg_begin + i].k_begin);
         items.push_back(it);
       }
+  // The attention kernel deals the list to its CTAs in rounds (snake order): sorted by falling
+  // cost, every CTA gets a similar total.  A step with one tile takes about 6/7 of a step with two.
+  std::stable_sort(items.begin(), items.end(), [](const ExtItem& a, const ExtItem& b) {
+    return attn_cost(a) > attn_cost(b);
+  });
   if (items.size() > (size_t)INT32_MAX) return fail(RX_ERR_RANGE, "plan too large");
 
   PlanHeader h;

@@ -65,6 +65,9 @@ struct ExtSeg {
   int32_t owner;        // -1 = all rows of the item
 };
 
+// Keys per step of the tensor-core attention kernel.
+constexpr int kAttnKeys = 64;
+
 // Two row tiles (A, B) of the same KV head that walk the same key segments: every K/V step feeds
 // 256 query rows.  Tile B may be empty (n_tok[1] == 0: the CTA runs tile A alone).  The same
 // kernel serves a decode plan's shared-prefix units with many query rows: its rows are then
@@ -76,7 +79,7 @@ struct ExtItem {
   int32_t seg_begin;     // into ext_segs: the union of both tiles' segments
   int32_t n_seg;
   int32_t kv_head;
-  int32_t pad;
+  int32_t n_steps;       // 64-key steps over the segments (each segment's keys rounded up)
   int32_t part[2];       // decode plans: first partial row of each tile; unused for extend
 };
 

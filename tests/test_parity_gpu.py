@@ -189,6 +189,31 @@ def test_decode_grouping_does_not_change_the_result(cuda):
     assert (l2 - dw.steps[0].dec_lse).abs().max().item() <= LSE_ABS
 
 
+def test_extend_output_only_16_byte_aligned(cuda):
+    """o at a 16-byte (not 32-byte) boundary: the kernel writes rows in 16-byte pieces there."""
+    wl = W.extend_workload(15, 8, 2, n_groups=2, members=3, prefix=300, ext_lo=20, ext_hi=150)
+    dw = DeviceWorkload(wl, cuda)
+    dw.run_step(0)
+    torch.cuda.synchronize()
+    st = dw.steps[0]
+    ref_o = st.ext_o.clone()
+    ref_l = st.ext_lse.clone()
+    n = ref_o.numel()
+    buf = torch.empty(n + 64, dtype=torch.bfloat16, device=cuda)
+    o16 = buf[8:8 + n].view_as(ref_o)  # 16 bytes past a 256-byte aligned base
+    assert o16.data_ptr() % 32 == 16
+    l2 = torch.empty_like(ref_l)
+    rx.extend_attn(st.ext_plan, dw.desc, dw.k_pool, dw.v_pool, st.ext_q, o16, l2, st.ext_ws)
+    torch.cuda.synchronize()
+    assert torch.equal(o16, ref_o)
+    assert torch.equal(l2, ref_l)
+    e = wl.steps[0].extend
+    kp, vp = oracle_pools(wl, 0)
+    o, l = A.extend(e.q, kp, vp, wl.req_to_token, e.req_idx, e.prefix_len, e.extend_len, e.cu_q,
+                    wl.softmax_scale)
+    assert_close(o16, l2, o, l, None, "extend, o 16-byte aligned")
+
+
 # ---------------------------------------------------------------------------------------------
 # Prefix trees (rx_decode_plan_tree / rx_extend_plan_tree): every node read once for the requests
 # beneath it, partials of all levels merged; the result is the plain definition's.
