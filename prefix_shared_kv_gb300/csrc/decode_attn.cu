@@ -352,13 +352,18 @@ int launch_decode(const rx_kv_desc* d, const PlanHeader* h, const void* k_pool,
       if (ce == cudaSuccess) ce = cudaEventCreateWithFlags(&a.join, cudaEventDisableTiming);
       if (ce != cudaSuccess) return (int)ce;
     }
+    // The tensor-core kernel takes whole SMs (one CTA fills an SM's shared memory), so it goes
+    // first, on the caller's stream with nothing to wait for; the mma.sync units follow on the
+    // second stream and fill the other SMs.
     ce = cudaEventRecord(a.fork, s);
-    if (ce == cudaSuccess) ce = cudaStreamWaitEvent(a.stream, a.fork, 0);
     if (ce != cudaSuccess) return (int)ce;
-    const int e = run_x(a.stream);
+    const int e = run_x(s);
     if (e) return e;
-    decode_partial_kernel<<<h->n_items, kThreads, kDecSmemBytes, s>>>(p);
-    ce = cudaEventRecord(a.join, a.stream);
+    ce = cudaStreamWaitEvent(a.stream, a.fork, 0);
+    if (ce != cudaSuccess) return (int)ce;
+    decode_partial_kernel<<<h->n_items, kThreads, kDecSmemBytes, a.stream>>>(p);
+    ce = cudaGetLastError();
+    if (ce == cudaSuccess) ce = cudaEventRecord(a.join, a.stream);
     if (ce == cudaSuccess) ce = cudaStreamWaitEvent(s, a.join, 0);
     if (ce != cudaSuccess) return (int)ce;
   } else if (h->n_xitems > 0) {

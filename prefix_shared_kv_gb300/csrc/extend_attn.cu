@@ -341,9 +341,11 @@ __device__ __forceinline__ void mma_issuer(const ExtParams& p, int x, uint32_t b
     for (int t = 0; ok && t < ntiles; ++t) {
       const uint32_t gt = gs + t, gt2 = gt + 2;
       const bool more = t + 2 < ntiles;
-      if (!wait(B_P_FULL + 2 * x + ((pb + t) & 1), ((pb + t) >> 1) & 1) ||
+      // the ring stages normally land long before the softmax hands P over: test them first, so
+      // only the P wait stands between P and the MMAs
+      if ((more && !wait(B_K_FULL + gt2 % kStages, (gt2 / kStages) & 1)) ||
           !wait(B_V_FULL + gt % kStages, (gt / kStages) & 1) ||
-          (more && !wait(B_K_FULL + gt2 % kStages, (gt2 / kStages) & 1)))
+          !wait(B_P_FULL + 2 * x + ((pb + t) & 1), ((pb + t) >> 1) & 1))
         break;
       tc::fence_after();
       pv(t);
@@ -486,7 +488,10 @@ __device__ __forceinline__ bool softmax_steps(const ExtParams& p, const ExtItem&
   const int x = threadIdx.x >> 7;  // tile: 0 = A, 1 = B
   const uint32_t col_o = kColO + x * 128;
   const float sl2 = p.scale_log2;
-  TileIter cur{0, segs[0].k_begin};
+  // the current key segment lives in registers; the next one's record is loaded when a segment
+  // starts, so no step waits for a table read
+  int seg = 0, k0 = segs[0].k_begin, k_end = segs[0].k_end, s_owner = segs[0].owner;
+  ExtSeg nsg = segs[it.n_seg > 1 ? 1 : 0];
   if (two && x == 1) tc::mbar_arrive(bar + 8 * B_TURN);  // tile A goes first
   // (a lone tile A takes no turns)
   for (int t = 0; t < ntiles; ++t) {
@@ -498,10 +503,9 @@ __device__ __forceinline__ bool softmax_steps(const ExtParams& p, const ExtItem&
     tc::fence_after();
     if (t == 0) ahead();
     if (t == ntiles - 1) prefetch();
-    const ExtSeg sg = segs[cur.seg];
-    const bool vis = row.valid && (sg.owner < 0 || sg.owner == row.owner);
-    const int lim = vis ? min(row.kmax, sg.k_end) : 0;  // keys at positions >= lim are masked
-    const int n_ok = max(0, min(kN, lim - cur.k0));
+    const bool vis = row.valid && (s_owner < 0 || s_owner == row.owner);
+    const int lim = vis ? min(row.kmax, k_end) : 0;  // keys at positions >= lim are masked
+    const int n_ok = max(0, min(kN, lim - k0));
     uint32_t sr[2][32];
     tc::ld32(lane_t + col_s, sr[0]);
     tc::ld32(lane_t + col_s + 32, sr[1]);
@@ -559,7 +563,13 @@ __device__ __forceinline__ bool softmax_steps(const ExtParams& p, const ExtItem&
     tc::wait_st();
     tc::fence_before();
     tc::mbar_arrive(bar + 8 * (B_P_FULL + 2 * x + ((c.pb + t) & 1)));
-    tile_next(cur, segs, it.n_seg);
+    k0 += kN;
+    if (k0 >= k_end && ++seg < it.n_seg) {
+      k0 = nsg.k_begin;
+      k_end = nsg.k_end;
+      s_owner = nsg.owner;
+      if (seg + 1 < it.n_seg) nsg = segs[seg + 1];
+    }
   }
   return true;
 }
