@@ -491,9 +491,15 @@ def run_e2e(wl, dw, dev, args, pg, world, w, unit, scale, has_ext):
             dc = st.decode
             rx.decode_plan(dplan[b], dw.desc, dc.req_idx, dc.seq_len, dc.group_of_req,
                            dc.group_prefix_len, dc.group_parent)
-        # H2D into set b once the kernels of the step that last used it are done
+        # H2D into set b once the kernels of the step that last used it are done: the plans first,
+        # then the inputs, all on the input stream (a plan upload queued on the kernel stream would
+        # wait behind the next step's input copy on the same copy engine)
         if issued[b]:
             s_in.wait_event(ev_cmp[b])
+        if st.extend is not None:
+            eplan[b].upload(ews[b], stream=s_in)
+        if st.decode is not None:
+            dplan[b].upload(dws[b], stream=s_in)
         with torch.cuda.stream(s_in):
             for k in h_in:
                 d_in[b][k].copy_(h_in[k], non_blocking=True)
@@ -505,11 +511,9 @@ def run_e2e(wl, dw, dev, args, pg, world, w, unit, scale, has_ext):
         rx.store_kv(dw.desc, dw.k_pool, dw.v_pool, d_in[b]["k_new"], d_in[b]["v_new"],
                     d_in[b]["slots"], stream=s_cmp)
         if st.extend is not None:
-            eplan[b].upload(ews[b], stream=s_cmp)
             rx.extend_attn(eplan[b], dw.desc, dw.k_pool, dw.v_pool, d_in[b]["ext_q"],
                            d_out[b]["ext_o"], d_out[b]["ext_lse"], ews[b], stream=s_cmp)
         if st.decode is not None:
-            dplan[b].upload(dws[b], stream=s_cmp)
             rx.decode_attn(dplan[b], dw.desc, dw.k_pool, dw.v_pool, d_in[b]["dec_q"],
                            d_out[b]["dec_o"], d_out[b]["dec_lse"], dws[b], stream=s_cmp)
         ev_cmp[b].record(s_cmp)
