@@ -98,8 +98,11 @@ void rx_plan_destroy(rx_plan* plan);
 /* Bytes of device workspace the built plan needs (tables + partial results). */
 rx_status rx_plan_workspace_size(const rx_plan* plan, size_t* bytes);
 /* Copy the plan's tables into `workspace` (device, >= rx_plan_workspace_size bytes, 256-byte
- * aligned) with cudaMemcpyAsync on `stream`.  The plan object may be rebuilt or destroyed as soon
- * as this returns. */
+ * aligned) with cudaMemcpyAsync on `stream`.  The tables are first copied into a pinned host
+ * buffer the plan owns, so the call returns without waiting for `stream`; a later upload of the
+ * same plan waits (on the host) for this copy to finish before reusing that buffer.  The plan
+ * object may be rebuilt or destroyed as soon as this returns (destroying it waits for its last
+ * copy). */
 rx_status rx_plan_upload(const rx_plan* plan, void* workspace, size_t workspace_bytes,
                          rx_stream_t stream);
 

@@ -91,6 +91,20 @@ struct rx_plan {
   int32_t hq = 0, hkv = 0;
   int64_t rows = 0, stride = 0, pool = 0;
   const int32_t* table = nullptr;
+  // rx_plan_upload stages the blob in pinned host memory so that the copy is asynchronous for the
+  // host too; `staged` records the copy, and the buffer is reused only once it has completed
+  mutable void* pinned = nullptr;
+  mutable size_t pinned_bytes = 0;
+  mutable cudaEvent_t staged = nullptr;
+  mutable int staged_dev = -1;
+  mutable bool staged_pending = false;
+  ~rx_plan() {
+    if (staged) {
+      if (staged_pending) cudaEventSynchronize(staged);
+      cudaEventDestroy(staged);
+    }
+    if (pinned) cudaFreeHost(pinned);
+  }
   PlanHeader hdr() const {
     PlanHeader h;
     std::memcpy(&h, blob.data(), sizeof h);
@@ -229,9 +243,41 @@ rx_status rx_plan_upload(const rx_plan* plan, void* workspace, size_t workspace_
   if (workspace_bytes < plan->ws_bytes)
     return fail(RX_ERR_WORKSPACE, "workspace of %zu bytes < %zu needed", workspace_bytes,
                 plan->ws_bytes);
-  cudaError_t e = cudaMemcpyAsync(workspace, plan->blob.data(), plan->blob.size(),
-                                  cudaMemcpyHostToDevice, (cudaStream_t)stream);
-  return e ? cuda_fail(e, "plan upload") : RX_OK;
+  // the previous upload's copy out of the staging buffer must be done before it is overwritten
+  cudaError_t e = cudaSuccess;
+  if (plan->staged_pending) {
+    e = cudaEventSynchronize(plan->staged);
+    if (e) return cuda_fail(e, "plan upload");
+    plan->staged_pending = false;
+  }
+  const size_t n = plan->blob.size();
+  if (plan->pinned_bytes < n) {
+    if (plan->pinned) cudaFreeHost(plan->pinned);
+    plan->pinned = nullptr;
+    plan->pinned_bytes = 0;
+    e = cudaHostAlloc(&plan->pinned, n, cudaHostAllocPortable);
+    if (e) return cuda_fail(e, "plan upload: pinned staging buffer");
+    plan->pinned_bytes = n;
+  }
+  int dev = 0;
+  e = cudaGetDevice(&dev);
+  if (e) return cuda_fail(e, "plan upload");
+  if (plan->staged && plan->staged_dev != dev) {  // events belong to one device
+    cudaEventDestroy(plan->staged);
+    plan->staged = nullptr;
+  }
+  if (!plan->staged) {
+    e = cudaEventCreateWithFlags(&plan->staged, cudaEventDisableTiming);
+    if (e) return cuda_fail(e, "plan upload");
+    plan->staged_dev = dev;
+  }
+  std::memcpy(plan->pinned, plan->blob.data(), n);
+  e = cudaMemcpyAsync(workspace, plan->pinned, n, cudaMemcpyHostToDevice, (cudaStream_t)stream);
+  if (e) return cuda_fail(e, "plan upload");
+  e = cudaEventRecord(plan->staged, (cudaStream_t)stream);
+  if (e) return cuda_fail(e, "plan upload");
+  plan->staged_pending = true;
+  return RX_OK;
 }
 
 // ---------------------------------------------------------------------------------------------

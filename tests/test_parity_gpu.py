@@ -214,6 +214,36 @@ def test_extend_output_only_16_byte_aligned(cuda):
     assert_close(o16, l2, o, l, None, "extend, o 16-byte aligned")
 
 
+def test_plan_rebuilt_and_uploaded_again_while_the_first_copy_may_be_in_flight(cuda):
+    """rx_plan_upload stages the tables in a pinned buffer the plan owns: rebuilding the plan and
+    uploading it again on another stream must leave each workspace with its own tables."""
+    wl = W.decode_workload(16, 16, 4, n_groups=2, members=6, prefix=300, dist_lo=20, dist_hi=120)
+    dw = DeviceWorkload(wl, cuda)
+    dw.run_step(0)
+    torch.cuda.synchronize()
+    d = wl.steps[0].decode
+    half = len(d.req_idx) // 2
+    plan = rx.Plan()
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    outs = []
+    for sel, st in ((np.arange(half), s1), (np.arange(half, len(d.req_idx)), s2)):
+        rx.decode_plan(plan, dw.desc, d.req_idx[sel], d.seq_len[sel])
+        ws = torch.empty(plan.workspace_size(), dtype=torch.uint8, device=cuda)
+        q = dw.steps[0].dec_q[torch.as_tensor(sel, device=cuda)].contiguous()
+        o = torch.empty_like(q)
+        l = torch.empty((len(sel), wl.num_q_heads), dtype=torch.float32, device=cuda)
+        with torch.cuda.stream(st):
+            plan.upload(ws, stream=st)
+            rx.decode_attn(plan, dw.desc, dw.k_pool, dw.v_pool, q, o, l, ws, stream=st)
+        outs.append((sel, o, l, ws))
+    torch.cuda.synchronize()
+    kp, vp = oracle_pools(wl, 0)
+    for sel, o, l, _ in outs:
+        ro, rl = A.decode(d.q[sel], kp, vp, wl.req_to_token, d.req_idx[sel], d.seq_len[sel],
+                          wl.softmax_scale)
+        assert_close(o, l, ro, rl, None, "decode, plan rebuilt between uploads")
+
+
 # ---------------------------------------------------------------------------------------------
 # Prefix trees (rx_decode_plan_tree / rx_extend_plan_tree): every node read once for the requests
 # beneath it, partials of all levels merged; the result is the plain definition's.
