@@ -118,6 +118,7 @@ namespace {
 // units of a one-tile step (a step with both tiles takes about 7/6 of one).
 int32_t attn_steps(int64_t n) { return (int32_t)((n + kAttnKeys - 1) / kAttnKeys); }
 int64_t attn_cost(const ExtItem& it) { return (int64_t)it.n_steps * (it.n_tok[1] > 0 ? 7 : 6); }
+constexpr int64_t kCostClass = 4 * 7;  // four two-tile steps
 
 template <typename T>
 void put(std::vector<uint8_t>& blob, int64_t off, const std::vector<T>& v) {
@@ -742,9 +743,11 @@ rx_status rx_extend_plan_tree(rx_plan* plan, const rx_kv_desc* desc, int32_t bat
         items.push_back(it);
       }
   // The attention kernel deals the list to its CTAs in rounds (snake order): sorted by falling
-  // cost, every CTA gets a similar total.  A step with one tile takes about 6/7 of a step with two.
+  // cost, every CTA gets a similar total.  The sort is by cost classes four two-tile steps wide,
+  // and keeps the planned order (a unit's KV heads and tiles together) inside a class, so items
+  // that read the same prefix still tend to run at the same time and share it in L2.
   std::stable_sort(items.begin(), items.end(), [](const ExtItem& a, const ExtItem& b) {
-    return attn_cost(a) > attn_cost(b);
+    return attn_cost(a) / kCostClass > attn_cost(b) / kCostClass;
   });
   if (items.size() > (size_t)INT32_MAX) return fail(RX_ERR_RANGE, "plan too large");
 
