@@ -260,22 +260,48 @@ __global__ void __launch_bounds__(32 * kMergeWarps) decode_merge_kernel(
   const int b = (int)(task / hq), h = (int)(task % hq);
   const int hk = h / gq, g = h % gq;
   const int r_begin = merge_idx[b], r_end = merge_idx[b + 1];
+  // Two passes per chunk of up to 32 partitions: the lanes fetch one partition's reference and
+  // LSE each and agree on their maximum, so every weight is known before any row is read; the
+  // row reads are then independent of one another (no load waits for the one before).
   float mx = -CUDART_INF_F, tot = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int i = r_begin; i < r_end; ++i) {
-    const DecMergeRef rf = refs[i];
-    const int64_t idx = (int64_t)rf.part + (int64_t)hk * rf.rows_real + rf.row + g;
-    const float li = part_lse[idx];
-    if (li == -CUDART_INF_F) continue;  // an empty partition contributes nothing
-    const float4 v = *reinterpret_cast<const float4*>(part_o + idx * kHeadDim + lane * 4);
-    const float m_new = fmaxf(mx, li);
-    const float a = fast_exp2(mx - m_new), w = fast_exp2(li - m_new);  // exp2(-inf) = 0
-    tot = tot * a + w;
-    acc.x = acc.x * a + w * v.x;
-    acc.y = acc.y * a + w * v.y;
-    acc.z = acc.z * a + w * v.z;
-    acc.w = acc.w * a + w * v.w;
+  for (int c0 = r_begin; c0 < r_end; c0 += 32) {
+    const int i = c0 + lane;
+    int64_t idx = 0;
+    float li = -CUDART_INF_F;
+    if (i < r_end) {
+      const DecMergeRef rf = refs[i];
+      idx = (int64_t)rf.part + (int64_t)hk * rf.rows_real + rf.row + g;
+      li = part_lse[idx];
+    }
+    float cm = li;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, off));
+    const float m_new = fmaxf(mx, cm);
+    if (m_new == -CUDART_INF_F) continue;  // only empty partitions so far
+    const float a = fast_exp2(mx - m_new);  // exp2(-inf) = 0
+    const float w = li == -CUDART_INF_F ? 0.f : fast_exp2(li - m_new);  // empty: contributes 0
+    float ws = w;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) ws += __shfl_xor_sync(0xffffffffu, ws, off);
+    tot = tot * a + ws;
+    acc.x *= a;
+    acc.y *= a;
+    acc.z *= a;
+    acc.w *= a;
     mx = m_new;
+    const int cnt = min(32, r_end - c0);
+#pragma unroll 4
+    for (int j = 0; j < cnt; ++j) {
+      const float wj = __shfl_sync(0xffffffffu, w, j);
+      const int64_t ij = __shfl_sync(0xffffffffu, idx, j);
+      if (wj == 0.f) continue;  // the same for the whole warp
+      const float4 v = *reinterpret_cast<const float4*>(part_o + ij * kHeadDim + lane * 4);
+      acc.x += wj * v.x;
+      acc.y += wj * v.y;
+      acc.z += wj * v.z;
+      acc.w += wj * v.w;
+    }
   }
   const float inv = tot > 0.f ? 1.f / tot : 0.f;
   __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
