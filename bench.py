@@ -36,6 +36,8 @@ if ROOT not in sys.path:
 
 METRIC = "prefix-shared attn: decode KV GB/s (% HBM peak); extend TFLOP/s (% BF16 peak)"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# nominal GB300 figures, reported beside the measured denominators (context only)
+NOMINAL_HBM_GBS, NOMINAL_BF16_TFLOPS = 8000.0, 2250.0
 
 
 # ---------------------------------------------------------------------------------------------
@@ -361,14 +363,19 @@ def main():
     if "store" in part_ms:
         a = w["store_bytes"] / (part_ms["store"] * 1e-3) / 1e9
         pdesc["store"] = {"ms": part_ms["store"], "GB/s": a, "frac_hbm": a / peaks["hbm_gbs"],
-                          "bytes": w["store_bytes"]}
+                          "frac_hbm_nominal": a / NOMINAL_HBM_GBS, "bytes": w["store_bytes"]}
     if has_ext:
         a = w["extend_flops"] / (part_ms["extend"] * 1e-3) / 1e12
         pdesc["extend"] = {"ms": part_ms["extend"], "TFLOP/s": a,
-                           "frac_bf16": a / peaks["bf16_tflops"], "flops": w["extend_flops"]}
+                           "frac_bf16": a / peaks["bf16_tflops"],
+                           "frac_bf16_sustained": a / peaks.get("bf16_tflops_sustained",
+                                                                peaks["bf16_tflops"]),
+                           "frac_bf16_nominal": a / NOMINAL_BF16_TFLOPS,
+                           "flops": w["extend_flops"]}
     if has_dec:
         a = w["decode_kv_bytes"] / (part_ms["decode"] * 1e-3) / 1e9
         pdesc["decode"] = {"ms": part_ms["decode"], "GB/s": a, "frac_hbm": a / peaks["hbm_gbs"],
+                           "frac_hbm_nominal": a / NOMINAL_HBM_GBS,
                            "unique_kv_bytes": w["decode_kv_bytes"],
                            # what the plan's kernels read (a prefix read for two member tiles of
                            # a group counts twice): the kernel's own bandwidth is plan bytes / ms

@@ -426,6 +426,53 @@ def tree_workload(seed: int, num_q_heads: int, num_kv_heads: int, *, depth: int,
 # The five named workloads.
 # --------------------------------------------------------------------------------------------
 
+def chunked_prefill_workload(seed: int, num_q_heads: int, num_kv_heads: int, *, system: int,
+                             prompt: int, chunk: int, n_decode: int, tail_lo: int, tail_hi: int,
+                             name: str = "chunked-prefill") -> Workload:
+    """Mixed token batching with chunked prefill: after a cached system prompt of `system` tokens,
+    one request's `prompt`-token prompt is prefilled `chunk` tokens per step; in every step
+    `n_decode` running requests (the same system prompt, then an own cached tail of U[tail_lo,
+    tail_hi] tokens) decode one token each.  A chunk is an extend whose prefix is the system prompt
+    plus the chunks before it, so each step's extend attends over everything already computed."""
+    rng = np.random.default_rng(seed)
+    n_steps = (prompt + chunk - 1) // chunk
+    pool = system + prompt + n_decode * (tail_hi + n_steps) + 64
+    pool = max(4096, (pool + 1023) // 1024 * 1024)
+    b = Builder(rng, num_q_heads, num_kv_heads, pool)
+    sp = b.cached(system)
+    chunks = [b.new(min(chunk, prompt - i * chunk)) for i in range(n_steps)]
+    tails = [b.cached(int(rng.integers(tail_lo, tail_hi + 1))) for _ in range(n_decode)]
+    dec_new = [[b.new(1) for _ in range(n_steps)] for _ in range(n_decode)]
+    long_row = b.row([sp] + chunks)
+    dec_rows = [b.row([sp, tails[j]] + dec_new[j]) for j in range(n_decode)]
+    steps = []
+    for st in range(n_steps):
+        done = system + sum(len(c.slots) for c in chunks[:st])
+        new_runs = [chunks[st]] + [dec_new[j][st] for j in range(n_decode)]
+        ext = ([long_row], [done], [len(chunks[st].slots)], [0], [done],
+               [_tokens([sp] + chunks[:st + 1])])
+        seq = [system + len(tails[j].slots) + st + 1 for j in range(n_decode)]
+        dec = (dec_rows, seq, [0] * n_decode, [system]) if n_decode else None
+        steps.append((new_runs, ext, dec))
+    cached = [(sp.tokens.copy(), sp.slots.copy())]
+    for j in range(n_decode):
+        cached.append((_tokens([sp, tails[j]]), _slots([sp, tails[j]])))
+    return b.finish(name, steps, cached,
+                    f"seed {seed}; Hq={num_q_heads} Hkv={num_kv_heads} d=128; cached system prompt "
+                    f"{system}; one {prompt}-token prompt prefilled {chunk} tokens per step over "
+                    f"{n_steps} steps; {n_decode} decode requests (system prompt + own tail "
+                    f"U[{tail_lo},{tail_hi}]) decode one token per step; pool {pool} slots, "
+                    f"random permutation")
+
+
+def llama3_chunked_prefill(seed: int = 1006) -> Workload:
+    """32 q / 8 kv heads; a 6144-token prompt prefilled 2048 tokens per step beside 64 decode
+    requests on a shared 1024-token system prompt (own tails U[200,1000])."""
+    return chunked_prefill_workload(seed, 32, 8, system=1024, prompt=6144, chunk=2048,
+                                    n_decode=64, tail_lo=200, tail_hi=1000,
+                                    name="llama3-chunked-prefill-6144x2048-64dec")
+
+
 def tiny(seed: int = 1001) -> Workload:
     """8 q / 2 kv heads; one cached 1000-token prefix in a 4096-slot pool; 4 requests extend 40
     new tokens each (causal), then 8 decode steps of one token per request."""
@@ -529,4 +576,5 @@ NAMED = {
     "gqa-decode": llama3_gqa_decode,
     "radix-mixed": radix_mixed,
     "radix-mixed-1level": lambda: radix_mixed(tree=False),
+    "chunked-prefill": llama3_chunked_prefill,
 }

@@ -376,3 +376,27 @@ def test_merge_gain_counts_tokens_saved_by_sharing_a_node():
             s.insert(t, list(range(len(t))))
         unshared = leaves * (tokens + 1)
         assert unshared - processed == accounting.merge_gain(leaves, tokens)
+
+
+def test_chunked_prefill_equals_one_prefill_of_the_whole_prompt():
+    """Chunked prefill (each chunk an extend over the system prompt and the chunks before it,
+    stored step by step) gives, row for row, what one extend of the whole prompt gives."""
+    wl = W.chunked_prefill_workload(7, 4, 2, system=96, prompt=300, chunk=128, n_decode=2,
+                                    tail_lo=5, tail_hi=20)
+    kp, vp = wl.k_pool, wl.v_pool
+    rows_o, rows_l, qs = [], [], []
+    for st in wl.steps:
+        kp, vp = A.store_kv(kp, vp, st.k_new, st.v_new, st.store_slots)
+        e = st.extend
+        o, l = A.extend(e.q, kp, vp, wl.req_to_token, e.req_idx, e.prefix_len, e.extend_len,
+                        e.cu_q, wl.softmax_scale)
+        rows_o.append(o)
+        rows_l.append(l)
+        qs.append(e.q)
+    assert [int(s.extend.prefix_len[0]) for s in wl.steps] == [96, 224, 352]
+    q = np.concatenate(qs)
+    ridx = wl.steps[0].extend.req_idx
+    o_full, l_full = A.extend(q, kp, vp, wl.req_to_token, ridx, np.array([96]), np.array([300]),
+                              np.array([0, 300]), wl.softmax_scale)
+    np.testing.assert_allclose(np.concatenate(rows_o), o_full, atol=1e-12)
+    np.testing.assert_allclose(np.concatenate(rows_l), l_full, atol=1e-12)

@@ -244,6 +244,15 @@ def test_plan_rebuilt_and_uploaded_again_while_the_first_copy_may_be_in_flight(c
         assert_close(o, l, ro, rl, None, "decode, plan rebuilt between uploads")
 
 
+@pytest.mark.parametrize("hq,hkv,chunk", [(8, 2, 512), (16, 16, 256)])
+def test_chunked_prefill_mixed_with_decode(cuda, hq, hkv, chunk):
+    """A long prompt prefilled chunk by chunk (each chunk an extend over the system prompt and the
+    earlier chunks) beside decode requests that share the system prompt, every step checked."""
+    wl = W.chunked_prefill_workload(8, hq, hkv, system=256, prompt=1200, chunk=chunk,
+                                    n_decode=6, tail_lo=20, tail_hi=120)
+    run_and_check(wl, cuda)
+
+
 # ---------------------------------------------------------------------------------------------
 # Prefix trees (rx_decode_plan_tree / rx_extend_plan_tree): every node read once for the requests
 # beneath it, partials of all levels merged; the result is the plain definition's.
@@ -308,7 +317,7 @@ def test_block_granular_pool(cuda, hq, hkv, prefix):
 # ---------------------------------------------------------------------------------------------
 
 @pytest.mark.parametrize("name", ["extend", "decode", "gqa-decode", "radix-mixed",
-                                  "radix-mixed-1level"])
+                                  "radix-mixed-1level", "chunked-prefill"])
 def test_full_size_workloads_sampled(cuda, name):
     wl = W.NAMED[name]()
     run_and_check(wl, cuda, sample=6, seed=1)
