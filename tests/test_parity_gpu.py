@@ -138,6 +138,14 @@ def test_extend_long_causal_and_empty(cuda):
     run_and_check(wl, cuda)
 
 
+def test_extend_very_long_prefix(cuda):
+    """Items of ~500 steps: a 32,000-token shared prefix (three members, GQA 4) and an ungrouped
+    request on its own 20,000-token prefix."""
+    wl = W.extend_workload(10, 8, 2, n_groups=1, members=3, prefix=32000, ext_lo=1, ext_hi=40,
+                           ungrouped=1, ungrouped_prefix=20000)
+    run_and_check(wl, cuda)
+
+
 def test_extend_peaky_softmax(cuda):
     wl = W.extend_workload(9, 8, 2, n_groups=1, members=4, prefix=200, ext_lo=30, ext_hi=90)
     for st in wl.steps:
@@ -162,6 +170,13 @@ def test_decode_long_prefix_many_chunks(cuda):
     run_and_check(wl, cuda)
     wl = W.decode_workload(12, 32, 8, n_groups=1, members=1, prefix=5000, dist_lo=1, dist_hi=1)
     run_and_check(wl, cuda)
+
+
+def test_decode_more_than_32_partials_per_request(cuda):
+    """An 80,000-token GQA prefix read in ~2,048-key chunks: ~40 partial rows per request, more
+    than one 32-partial chunk of the merge."""
+    wl = W.decode_workload(14, 32, 8, n_groups=1, members=8, prefix=80000, dist_lo=1, dist_hi=50)
+    run_and_check(wl, cuda, sample=3, seed=2)
 
 
 def test_decode_group_prefix_zero_and_ungrouped_only(cuda):
