@@ -369,7 +369,9 @@ rx_status rx_decode_plan_tree(rx_plan* plan, const rx_kv_desc* desc, int32_t bat
                ((members[g].size() + max_tok - 1) / max_tok);
   for (int b = 0; b < batch; ++b)
     total += (double)(seq_len[b] - (grp[b] >= 0 ? group_prefix_len[grp[b]] : 0)) * hkv * key_bytes;
-  const double target = std::min(4.0 * 1048576, std::max(256.0 * 1024, total / (3.0 * device_sms())));
+  // bytes of K/V per mma.sync item: about three items per SM, but no item under 1 MiB (smaller
+  // ones spend more on their own start and partial write-out than on the read)
+  const double target = std::min(4.0 * 1048576, std::max(1048576.0, total / (3.0 * device_sms())));
 
   auto chunks = [&](int len, int kind, std::vector<std::pair<int, int>>& out) {
     const int hb = std::min(hb_of(kind), hkv);
