@@ -150,7 +150,7 @@ def kv_desc(num_q_heads: int, num_kv_heads: int, pool_size: int, req_to_token,
     if softmax_scale is None:
         softmax_scale = head_dim ** -0.5
     rows, stride = (req_to_token.shape if req_to_token is not None else (0, 0))
-    if req_to_token is not None and req_to_token.stride(1) != 1:
+    if req_to_token is not None and req_to_token.numel() > 0 and req_to_token.stride(1) != 1:
         raise ValueError("req_to_token rows must be contiguous")
     return KVDesc(num_q_heads, num_kv_heads, head_dim, softmax_scale, pool_size,
                   _ptr(req_to_token), rows, req_to_token.stride(0) if req_to_token is not None else 0)

@@ -163,9 +163,10 @@ class Builder:
         placed at randomly permuted req_to_token indices."""
         n_rows = len(self.rows)
         width = max([len(r) for r in self.rows] + [1])
+        table_rows = max(n_rows, 1)  # the library wants a table of at least one row
         width = (width + 15) // 16 * 16
         row_perm = self.rng.permutation(n_rows).astype(np.int32)
-        r2t = np.zeros((n_rows, width), dtype=np.int32)
+        r2t = np.zeros((table_rows, width), dtype=np.int32)
         for i, r in enumerate(self.rows):
             r2t[row_perm[i], :len(r)] = r
         steps = []
@@ -224,7 +225,7 @@ def extend_workload(seed: int, num_q_heads: int, num_kv_heads: int, *, n_groups:
     ext = rng.integers(ext_lo, ext_hi + 1, size=n_req)
     own = rng.integers(0, own_cached_hi + 1, size=n_req) if own_cached_hi > 0 else np.zeros(n_req, np.int64)
     need = n_groups * prefix + int(ext.sum()) + int(own.sum()) + ungrouped * ungrouped_prefix
-    P = pool_size if pool_size is not None else max(4096, 1 << int(np.ceil(np.log2(need * 1.25))))
+    P = pool_size if pool_size is not None else max(4096, 1 << int(np.ceil(np.log2(need * 1.25 + 1))))
     b = Builder(rng, num_q_heads, num_kv_heads, P)
     rows, pl, grp, toks, new_runs, cached_seqs = [], [], [], [], [], []
     gpl = []
@@ -275,7 +276,7 @@ def decode_workload(seed: int, num_q_heads: int, num_kv_heads: int, *, n_groups:
     n_req = n_groups * members + ungrouped
     dist = rng.integers(dist_lo, dist_hi + 1, size=n_req)
     need = n_groups * prefix + int(dist.sum())
-    P = max(min_pool, need) if min_pool else max(4096, 1 << int(np.ceil(np.log2(need * 1.25))))
+    P = max(min_pool, need) if min_pool else max(4096, 1 << int(np.ceil(np.log2(need * 1.25 + 1))))
     b = Builder(rng, num_q_heads, num_kv_heads, P)
     rows, sl, grp, gpl, new_runs, cached_seqs = [], [], [], [], [], []
     i = 0
@@ -319,7 +320,7 @@ def paged_workload(seed: int, num_q_heads: int, num_kv_heads: int, *, page: int,
     shared = prefix // page * page
     ext = rng.integers(ext_lo, ext_hi + 1, size=n_req)
     need_pages = shared // page + int(sum((prefix - shared + e + 1 + page - 1) // page + 1 for e in ext))
-    P = max(4096, 1 << int(np.ceil(np.log2(need_pages * page * 1.25))))
+    P = max(4096, 1 << int(np.ceil(np.log2(need_pages * page * 1.25 + 1))))
     b = Builder(rng, num_q_heads, num_kv_heads, P, page=page)
     pre = b.cached(shared) if shared > 0 else None
     cached_seqs = [(pre.tokens.copy(), pre.slots.copy())] if pre is not None else []

@@ -143,6 +143,15 @@ def test_plans_size_workspaces_without_a_gpu(librx):
     assert e.value.status == rx.RX_ERR_INVALID
 
 
+def test_empty_batches_plan_to_no_work(librx):
+    d = _desc(rows=1, stride=16, hq=4, hkv=2)
+    p = rx.Plan()
+    rx.extend_plan(p, d, [], [], [], [], [])
+    assert p.workspace_size() == 256 and p.key_reads() == 0  # the header alone
+    rx.decode_plan(p, d, [], [], [], [])
+    assert p.key_reads() == 0
+
+
 def test_tree_plan_argument_checks(librx):
     p = rx.Plan()
     d = _desc()

@@ -23,6 +23,9 @@ def assert_close(o_gpu, lse_gpu, o_ref, lse_ref, rows=None, what=""):
     l = lse_gpu.double().cpu().numpy()
     if rows is not None:
         o, l, o_ref, lse_ref = o[rows], l[rows], o_ref[rows], lse_ref[rows]
+    assert o.shape == o_ref.shape and l.shape == lse_ref.shape, what
+    if o_ref.size == 0:  # an empty batch: nothing to compare
+        return
     assert np.isfinite(o_ref).all()
     err = np.abs(o - o_ref)
     lerr = np.abs(l - lse_ref)
@@ -144,6 +147,14 @@ def test_extend_very_long_prefix(cuda):
     wl = W.extend_workload(10, 8, 2, n_groups=1, members=3, prefix=32000, ext_lo=1, ext_hi=40,
                            ungrouped=1, ungrouped_prefix=20000)
     run_and_check(wl, cuda)
+
+
+def test_empty_batches(cuda):
+    """No requests at all: plans with no items, calls that launch nothing and return OK."""
+    run_and_check(W.extend_workload(3, 4, 2, n_groups=0, members=3, prefix=100, ext_lo=1,
+                                    ext_hi=30, ungrouped=0), cuda)
+    run_and_check(W.decode_workload(3, 4, 2, n_groups=0, members=3, prefix=100, dist_lo=1,
+                                    dist_hi=30, ungrouped=0), cuda)
 
 
 def test_extend_peaky_softmax(cuda):
