@@ -368,3 +368,42 @@ def test_bounded_wait_times_out_and_the_context_stays_usable(cuda):
     torch.cuda.synchronize()
     assert status.item() == rx.RX_ERR_TIMEOUT
     run_and_check(W.tiny(), cuda)                        # kernels still run and agree
+
+
+# ---------------------------------------------------------------------------------------------
+# Random shapes: extend, decode and tree workloads with random head ratios, group sizes, prefix
+# and tail lengths (empty parts included), each checked against the oracle.
+# ---------------------------------------------------------------------------------------------
+
+def _random_workload(rng, i):
+    hkv = int(rng.choice([1, 2, 4, 8]))
+    hq = hkv * int(rng.choice([1, 2, 4, 8]))
+    seed = int(rng.integers(0, 1 << 30))
+    kind = i % 3
+    if kind == 0:
+        return W.extend_workload(seed, hq, hkv, n_groups=int(rng.integers(0, 4)),
+                                 members=int(rng.integers(1, 9)),
+                                 prefix=int(rng.integers(0, 1500)),
+                                 ext_lo=int(rng.integers(0, 30)), ext_hi=int(rng.integers(30, 300)),
+                                 own_cached_hi=int(rng.integers(0, 100)),
+                                 ungrouped=int(rng.integers(0, 4)),
+                                 ungrouped_prefix=int(rng.integers(0, 700)))
+    if kind == 1:
+        return W.decode_workload(seed, hq, hkv, n_groups=int(rng.integers(1, 4)),
+                                 members=int(rng.integers(1, 40)),
+                                 prefix=int(rng.integers(0, 5000)), dist_lo=1,
+                                 dist_hi=int(rng.integers(1, 800)),
+                                 ungrouped=int(rng.integers(0, 4)))
+    return W.tree_workload(seed, hq, hkv, depth=int(rng.integers(1, 5)),
+                           fanout=int(rng.integers(1, 4)), seg_lo=0,
+                           seg_hi=int(rng.integers(1, 600)), p_empty=float(rng.random() * 0.4),
+                           n_decode=int(rng.integers(1, 40)), tail_hi=int(rng.integers(0, 80)),
+                           n_extend=int(rng.integers(1, 12)), own_hi=int(rng.integers(0, 60)),
+                           ext_lo=int(rng.integers(1, 20)), ext_hi=int(rng.integers(20, 200)))
+
+
+@pytest.mark.parametrize("seed", [301, 302, 303])
+def test_random_workloads(cuda, seed):
+    rng = np.random.default_rng(seed)
+    for i in range(10):
+        run_and_check(_random_workload(rng, i), cuda)
