@@ -14,8 +14,10 @@
  * Conventions for every call
  * --------------------------
  *  Memory   All tensors are caller-owned.  Pointers marked (device) are CUDA device memory,
- *           (host) are ordinary host memory.  The library keeps no device allocation between
- *           calls; scratch ("workspace") is sized by the library and passed in by the caller.
+ *           (host) are ordinary host memory.  The library allocates no device memory: scratch
+ *           ("workspace") is sized by the library and passed in by the caller (the no-allocation
+ *           decode below uses a static array inside the library instead).  A plan owns a pinned
+ *           host buffer through which it is uploaded.
  *  Layout   bf16 tensors, row-major, 16-byte aligned:
  *             K pool, V pool   [pool_size, num_kv_heads, head_dim]   slot-major (page = 1 token)
  *             q, o             [rows, num_q_heads, head_dim]
@@ -122,7 +124,9 @@ rx_status rx_plan_upload(const rx_plan* plan, void* workspace, size_t workspace_
  * prefix_len[r]); the kernel then reads that prefix KV once for all new rows of the group.  -1 (or
  * group_of_req == NULL) declares no sharing.  The result does not depend on the grouping.
  * All arrays of rx_extend_plan are (host).  extend_len[r] == 0 is allowed; sum of extend_len must
- * be < 2^31.
+ * be < 2^31.  batch == 0 builds a plan with no work: the attention call then enqueues nothing and
+ * may be given NULL tensors.  o needs 16-byte alignment; at 32-byte alignment rows are written in
+ * 32-byte pieces.
  * ------------------------------------------------------------------------------------------- */
 rx_status rx_extend_plan(rx_plan* plan, const rx_kv_desc* desc, int32_t batch,
                          const int32_t* req_idx, const int32_t* prefix_len,
