@@ -214,6 +214,34 @@ rx_status rx_decode_attn_noalloc(const rx_plan* plan, const rx_kv_desc* desc, co
                                  const void* v_pool, const void* q, void* o, float* lse,
                                  rx_stream_t stream);
 
+/* ---------------------------------------------------------------------------------------------
+ * Validation (host; a checking mode for callers and debug builds).  The attention and store
+ * calls trust two contracts for speed: the shared prefixes a plan declares really are shared, and
+ * the slots a store writes are distinct.  These checks verify them on the host copies of the
+ * arrays the caller built (the radix match that fills the table runs on the CPU), before upload.
+ * Both are O(total keys); neither touches a GPU.  Each returns RX_OK, or on the first violation
+ * its code with a message (rx_last_error) naming the request / token, whose index goes to *bad
+ * (nullable; -1 when all is well or the arguments themselves are wrong).
+ *
+ * rx_check_slots: slots[0..n) (host) for rx_store_kv.  RX_ERR_RANGE for a slot outside
+ * [0, pool_size), RX_ERR_INVALID for a slot that repeats an earlier one.
+ * rx_check_tables: req_to_token (host) [rows, stride] int32; request b owns row req_idx[b] and
+ * reads key_len[b] keys (prefix_len + extend_len for extend, seq_len for decode); groups as for
+ * rx_extend_plan_tree / rx_decode_plan_tree (group_of_req and group_parent nullable).
+ * RX_ERR_RANGE: a row index, length or slot out of range, a request shorter than its group's
+ * prefix, or a forest that is not parent-first with growing prefixes.  RX_ERR_INVALID: the group
+ * contract is broken -- for some group g, two requests of g's subtree differ in one of the first
+ * group_prefix_len[g] entries of their rows (SGLang explainer, RadixAttention: requests that
+ * share a tree node share that node's KV pages; BatchLLM explainer, Global Prefix Sharing: a
+ * group's common prefix is one KV context).
+ * ------------------------------------------------------------------------------------------- */
+rx_status rx_check_slots(const int32_t* slots, int64_t n, int64_t pool_size, int64_t* bad);
+rx_status rx_check_tables(const int32_t* req_to_token, int64_t rows, int64_t stride,
+                          int64_t pool_size, int32_t batch, const int32_t* req_idx,
+                          const int32_t* key_len, const int32_t* group_of_req,
+                          int32_t num_groups, const int32_t* group_prefix_len,
+                          const int32_t* group_parent, int64_t* bad);
+
 /* Read (synchronously, on `stream`) and clear the device status word of a workspace that a plan
  * was uploaded to.  *status receives RX_OK or the first device-side error recorded. */
 rx_status rx_read_status(const void* workspace, int32_t* status, rx_stream_t stream);

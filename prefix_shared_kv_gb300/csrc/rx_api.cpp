@@ -806,4 +806,101 @@ rx_status rx_read_status(const void* workspace, int32_t* status, rx_stream_t str
   return RX_OK;
 }
 
+// ---------------------------------------------------------------------------------------------
+// Validation of the contracts the attention calls trust (host copies of the tables).
+// ---------------------------------------------------------------------------------------------
+rx_status rx_check_slots(const int32_t* slots, int64_t n, int64_t pool_size, int64_t* bad) {
+  if (bad) *bad = -1;
+  if (n < 0 || pool_size <= 0) return fail(RX_ERR_INVALID, "negative count or empty pool");
+  if (n > 0 && !slots) return fail(RX_ERR_INVALID, "slots is NULL");
+  for (int64_t t = 0; t < n; ++t)
+    if (slots[t] < 0 || slots[t] >= pool_size) {
+      if (bad) *bad = t;
+      return fail(RX_ERR_RANGE, "slots[%lld] = %d is outside the pool [0, %lld)", (long long)t,
+                  slots[t], (long long)pool_size);
+    }
+  // (slot, index) pairs in order: within a run of one slot the first index is the original and
+  // every later one a repeat; the earliest repeat over all runs is reported
+  std::vector<std::pair<int32_t, int64_t>> by(n);
+  for (int64_t t = 0; t < n; ++t) by[t] = {slots[t], t};
+  std::sort(by.begin(), by.end());
+  int64_t rep = -1, orig = -1, run = 0;  // run: start of the current slot's run
+  for (int64_t i = 1; i < n; ++i) {
+    if (by[i].first != by[i - 1].first) {
+      run = i;
+    } else if (i == run + 1 && (rep < 0 || by[i].second < rep)) {  // a run's first repeat
+      rep = by[i].second;
+      orig = by[run].second;
+    }
+  }
+  if (rep >= 0) {
+    if (bad) *bad = rep;
+    return fail(RX_ERR_INVALID, "slots[%lld] = %d repeats slots[%lld]", (long long)rep,
+                slots[rep], (long long)orig);
+  }
+  return RX_OK;
+}
+
+rx_status rx_check_tables(const int32_t* req_to_token, int64_t rows, int64_t stride,
+                          int64_t pool_size, int32_t batch, const int32_t* req_idx,
+                          const int32_t* key_len, const int32_t* group_of_req,
+                          int32_t num_groups, const int32_t* group_prefix_len,
+                          const int32_t* group_parent, int64_t* bad) {
+  if (bad) *bad = -1;
+  if (!req_to_token || rows <= 0 || stride <= 0 || pool_size <= 0 || batch < 0 ||
+      num_groups < 0)
+    return fail(RX_ERR_INVALID, "bad table shape, pool size or count");
+  if (batch > 0 && (!req_idx || !key_len)) return fail(RX_ERR_INVALID, "NULL length array");
+  if (num_groups > 0 && !group_prefix_len) return fail(RX_ERR_INVALID, "group_prefix_len NULL");
+  rx_status st = check_tree(num_groups, group_prefix_len, group_parent);
+  if (st) return st;
+  auto parent = [&](int g) { return group_parent ? group_parent[g] : -1; };
+  auto row = [&](int b) { return req_to_token + (int64_t)req_idx[b] * stride; };
+  // lengths and slots of every request
+  for (int b = 0; b < batch; ++b) {
+    if (bad) *bad = b;
+    if (req_idx[b] < 0 || req_idx[b] >= rows)
+      return fail(RX_ERR_RANGE, "req_idx[%d] = %d outside the table", b, req_idx[b]);
+    if (key_len[b] < 0 || key_len[b] > stride)
+      return fail(RX_ERR_RANGE, "request %d reads %d keys, table rows hold %lld", b, key_len[b],
+                  (long long)stride);
+    const int g = group_of_req ? group_of_req[b] : -1;
+    if (g < -1 || g >= num_groups) return fail(RX_ERR_RANGE, "group_of_req[%d] = %d", b, g);
+    if (g >= 0 && group_prefix_len[g] > key_len[b])
+      return fail(RX_ERR_RANGE, "request %d reads %d keys, fewer than its group's prefix %d", b,
+                  key_len[b], group_prefix_len[g]);
+    const int32_t* r = row(b);
+    for (int j = 0; j < key_len[b]; ++j)
+      if (r[j] < 0 || r[j] >= pool_size)
+        return fail(RX_ERR_RANGE, "request %d: key %d has slot %d outside the pool", b, j, r[j]);
+  }
+  // Every request holds, for each group a on its path, the same entries as a's first request
+  // (in batch order, over a's subtree) on a's own keys [prefix of a's parent, prefix of a).  By
+  // induction down the path, every request of a's subtree then agrees with every other on
+  // [0, prefix of a): the shared prefix the planners read once.
+  std::vector<int> rep(num_groups, -1);
+  for (int b = 0; b < batch; ++b) {
+    const int g = group_of_req ? group_of_req[b] : -1;
+    for (int a = g; a >= 0; a = parent(a))
+      if (rep[a] < 0) rep[a] = b;
+  }
+  for (int b = 0; b < batch; ++b) {
+    const int g = group_of_req ? group_of_req[b] : -1;
+    for (int a = g; a >= 0; a = parent(a)) {
+      const int lo = parent(a) >= 0 ? group_prefix_len[parent(a)] : 0;
+      const int32_t *x = row(b), *y = row(rep[a]);
+      for (int j = lo; j < group_prefix_len[a]; ++j)
+        if (x[j] != y[j]) {
+          if (bad) *bad = b;
+          return fail(RX_ERR_INVALID,
+                      "request %d, key %d: slot %d differs from slot %d of request %d, the "
+                      "first of group %d (a shared prefix of %d keys)",
+                      b, j, x[j], y[j], rep[a], a, group_prefix_len[a]);
+        }
+    }
+  }
+  if (bad) *bad = -1;
+  return RX_OK;
+}
+
 }  // extern "C"

@@ -23,20 +23,20 @@ EXPORTED = [
     "rx_status_string", "rx_last_error", "rx_store_kv", "rx_plan_create", "rx_plan_destroy",
     "rx_plan_workspace_size", "rx_plan_upload", "rx_plan_key_reads", "rx_extend_plan",
     "rx_extend_plan_tree", "rx_extend_attn", "rx_decode_plan", "rx_decode_plan_tree",
-    "rx_decode_attn", "rx_decode_attn_noalloc", "rx_read_status", "rx_selftest_wait_timeout", "rx_radix_create", "rx_radix_destroy",
+    "rx_decode_attn", "rx_decode_attn_noalloc", "rx_read_status", "rx_selftest_wait_timeout",
+    "rx_check_slots", "rx_check_tables", "rx_radix_create", "rx_radix_destroy",
     "rx_radix_insert", "rx_radix_match", "rx_radix_stats", "rx_radix_acquire", "rx_radix_release",
     "rx_radix_evict", "rx_slot_pool_create", "rx_slot_pool_destroy", "rx_slot_pool_free_count",
     "rx_slot_pool_alloc", "rx_slot_pool_release", "rx_dfs_order", "rx_gain_groups",
-    "rx_saved_tokens",
-    "rx_token_saving",
-    "rx_compute_reduction",
+    "rx_saved_tokens", "rx_token_saving", "rx_compute_reduction",
 ]
 
 
 class RxError(RuntimeError):
-    def __init__(self, status: int, msg: str):
+    def __init__(self, status: int, msg: str, bad: int = -1):
         super().__init__(f"{msg} (status {status})")
         self.status = status
+        self.bad = bad  # the offending index a check reported, else -1
 
 
 class KVDesc(C.Structure):
@@ -102,6 +102,9 @@ def lib():
         "rx_saved_tokens": (C.c_int64, [C.c_int64, C.c_int32]),
         "rx_token_saving": (C.c_double, [C.c_int64, C.c_int64]),
         "rx_compute_reduction": (C.c_double, [C.c_int64, C.c_int64]),
+        "rx_check_slots": (C.c_int, [_I32P, C.c_int64, C.c_int64, _I64P]),
+        "rx_check_tables": (C.c_int, [_I32P, C.c_int64, C.c_int64, C.c_int64, C.c_int32, _I32P,
+                                      _I32P, _I32P, C.c_int32, _I32P, _I32P, _I64P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -111,10 +114,11 @@ def lib():
     return L
 
 
-def _check(status: int):
+def _check(status: int, bad: int = -1):
     if status != RX_OK:
         L = lib()
-        raise RxError(status, f"{L.rx_status_string(status).decode()}: {L.rx_last_error().decode()}")
+        raise RxError(status, f"{L.rx_status_string(status).decode()}: {L.rx_last_error().decode()}",
+                      bad)
 
 
 def _ptr(t) -> int:
@@ -403,3 +407,34 @@ def token_saving(n_processed: int, n_logical: int) -> float:
 
 def compute_reduction(l_prefix: int, l_new: int) -> float:
     return lib().rx_compute_reduction(l_prefix, l_new)
+
+
+def check_slots(slots, pool_size: int):
+    """rx_check_slots: raises RxError (with .bad = the token) unless the host slots are distinct
+    and inside the pool."""
+    a, ap = _host_i32(slots)
+    bad = C.c_int64(-1)
+    st = lib().rx_check_slots(ap, int(a.shape[0]), int(pool_size), C.byref(bad))
+    _check(st, bad.value)
+
+
+def check_tables(req_to_token, pool_size: int, req_idx, key_len, group_of_req=None,
+                 group_prefix_len=None, group_parent=None):
+    """rx_check_tables on a host copy of req_to_token ([rows, stride] int32): raises RxError
+    (with .bad = the request) unless every slot a request reads is inside the pool and every
+    declared shared prefix is the same in all rows that declare it."""
+    t = req_to_token.cpu().numpy() if hasattr(req_to_token, "cpu") else req_to_token
+    t = np.ascontiguousarray(np.asarray(t, dtype=np.int32))
+    if t.ndim != 2:
+        raise ValueError("req_to_token must be [rows, stride]")
+    ri, rip = _host_i32(req_idx)
+    kl, klp = _host_i32(key_len)
+    g, gp_ = _host_i32(group_of_req)
+    gl, glp = _host_i32(group_prefix_len)
+    pa, pap = _host_i32(group_parent)
+    ng = 0 if gl is None else int(gl.shape[0])
+    bad = C.c_int64(-1)
+    st = lib().rx_check_tables(t.ctypes.data_as(_I32P), int(t.shape[0]), int(t.shape[1]),
+                               int(pool_size), int(ri.shape[0]), rip, klp, gp_, ng, glp, pap,
+                               C.byref(bad))
+    _check(st, bad.value)
