@@ -165,6 +165,45 @@ def test_extend_peaky_softmax(cuda):
     run_and_check(wl, cuda)
 
 
+def _unit_values(wl):
+    one = np.uint16(0x3F80)  # bf16 1.0
+    wl.v_pool = np.full_like(wl.v_pool, one)
+    for st in wl.steps:
+        st.v_new = np.full_like(st.v_new, one)
+    return wl
+
+
+def _within_one_ulp_of_one(o, what):
+    # bf16 neighbours of 1.0: 1 - 2^-8 below, 1 + 2^-7 above
+    v = A.bf16_to_f64(bits_of(o))
+    assert v.size > 0 and ((v >= 1 - 2 ** -8) & (v <= 1 + 2 ** -7)).all(), \
+        f"{what}: O in [{v.min()}, {v.max()}]"
+
+
+@pytest.mark.parametrize("kind", ["extend", "decode", "tree"])
+def test_unit_values_give_unit_output(cuda, kind):
+    """With every V row equal to 1 the attention weights of a row sum to one, so each output is
+    1.0 to one bf16 unit: this pins the kernels' own normalisation (P rounded to bf16 for the PV
+    product against the fp32 row sum; partial rows merged by LSE), whatever the scores are."""
+    if kind == "extend":
+        wl = W.extend_workload(31, 16, 4, n_groups=2, members=6, prefix=900, ext_lo=1,
+                               ext_hi=160, own_cached_hi=40, ungrouped=2, ungrouped_prefix=300)
+    elif kind == "decode":
+        # 24 members x gq 4 stack 96 rows: the shared prefix goes through the tensor-core units
+        wl = W.decode_workload(32, 16, 4, n_groups=2, members=24, prefix=3000, dist_lo=1,
+                               dist_hi=400, ungrouped=3)
+    else:
+        wl = W.tree_workload(33, 8, 8, depth=3, fanout=3, seg_lo=0, seg_hi=300, p_empty=0.2,
+                             n_decode=30, tail_hi=60, n_extend=6, own_hi=40, ext_lo=1,
+                             ext_hi=120)
+    dw = run_and_check(_unit_values(wl), cuda)
+    for i, st in enumerate(wl.steps):
+        if st.extend is not None:
+            _within_one_ulp_of_one(dw.steps[i].ext_o, f"{kind} extend")
+        if st.decode is not None:
+            _within_one_ulp_of_one(dw.steps[i].dec_o, f"{kind} decode")
+
+
 # ---------------------------------------------------------------------------------------------
 # Decode: groups of many members, single-member groups, empty own parts, long prefixes.
 # ---------------------------------------------------------------------------------------------
