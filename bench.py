@@ -398,7 +398,13 @@ def main():
     roof["peak_source"] = f"{peak_src} (burst)" if roof["unit"] == "TFLOP/s" else peak_src
     roof["traffic"] = recorded_traffic(dom[1], wl.name)
 
-    launches_per_step = {"store": 1, "extend": 1, "decode": 2}
+    # kernels of ours per step, as the plans report them (a decode plan launches its tensor-core
+    # units, its mma.sync units and the merge)
+    st0 = dw.steps[0]
+    launches_per_step = {
+        "store": int(wl.steps[0].store_slots.shape[0] > 0),
+        "extend": st0.ext_plan.launches() if st0.ext_plan is not None else 0,
+        "decode": st0.dec_plan.launches() if st0.dec_plan is not None else 0}
     gpu_launches = args.steps * sum(launches_per_step[n] for n, _ in parts)
 
     # ---- end to end through the public API with host buffers -----------------------------

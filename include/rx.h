@@ -97,6 +97,10 @@ typedef struct rx_plan rx_plan;
 
 rx_status rx_plan_create(rx_plan** out);
 void rx_plan_destroy(rx_plan* plan);
+/* Number of kernels one attention call with the built plan launches (0 for a plan without work;
+ * a decode plan launches up to three: tensor-core shared-prefix units, mma.sync units, merge).
+ * For a caller's and a benchmark's bookkeeping; (host). */
+rx_status rx_plan_launches(const rx_plan* plan, int32_t* launches);
 /* Bytes of device workspace the built plan needs (tables + partial results). */
 rx_status rx_plan_workspace_size(const rx_plan* plan, size_t* bytes);
 /* Copy the plan's tables into `workspace` (device, >= rx_plan_workspace_size bytes, 256-byte

@@ -228,6 +228,18 @@ rx_status rx_plan_key_reads(const rx_plan* plan, int64_t* rows) {
   return RX_OK;
 }
 
+rx_status rx_plan_launches(const rx_plan* plan, int32_t* launches) {
+  if (!plan || !launches) return fail(RX_ERR_INVALID, "NULL argument");
+  if (!plan->kind) return fail(RX_ERR_INVALID, "plan has not been built");
+  const PlanHeader h = plan->hdr();
+  // the same conditions the launchers test: extend -- the tensor-core kernel when there are
+  // items; decode -- the tensor-core kernel for its shared-prefix units, the mma.sync partial
+  // kernel for the others, and the merge whenever there are requests
+  *launches = plan->kind == 1 ? (h.n_items > 0)
+                              : (h.n_xitems > 0) + (h.n_items > 0) + (h.batch > 0);
+  return RX_OK;
+}
+
 rx_status rx_plan_workspace_size(const rx_plan* plan, size_t* bytes) {
   if (!plan || !bytes) return fail(RX_ERR_INVALID, "NULL argument");
   if (!plan->kind) return fail(RX_ERR_INVALID, "plan has not been built");

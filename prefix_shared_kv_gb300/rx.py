@@ -21,7 +21,8 @@ RX_OK, RX_ERR_INVALID, RX_ERR_RANGE, RX_ERR_UNSUPPORTED, RX_ERR_CUDA, RX_ERR_TIM
 
 EXPORTED = [
     "rx_status_string", "rx_last_error", "rx_store_kv", "rx_plan_create", "rx_plan_destroy",
-    "rx_plan_workspace_size", "rx_plan_upload", "rx_plan_key_reads", "rx_extend_plan",
+    "rx_plan_workspace_size", "rx_plan_upload", "rx_plan_key_reads", "rx_plan_launches",
+    "rx_extend_plan",
     "rx_extend_plan_tree", "rx_extend_attn", "rx_decode_plan", "rx_decode_plan_tree",
     "rx_decode_attn", "rx_decode_attn_noalloc", "rx_read_status", "rx_selftest_wait_timeout",
     "rx_check_slots", "rx_check_tables", "rx_radix_create", "rx_radix_destroy",
@@ -69,6 +70,7 @@ def lib():
         "rx_plan_workspace_size": (C.c_int, [_P, C.POINTER(C.c_size_t)]),
         "rx_plan_upload": (C.c_int, [_P, _P, C.c_size_t, _P]),
         "rx_plan_key_reads": (C.c_int, [_P, _I64P]),
+        "rx_plan_launches": (C.c_int, [_P, _I32P]),
         "rx_extend_plan": (C.c_int, [_P, C.POINTER(KVDesc), C.c_int32, _I32P, _I32P, _I32P,
                                      _I32P, C.c_int32, _I32P]),
         "rx_extend_plan_tree": (C.c_int, [_P, C.POINTER(KVDesc), C.c_int32, _I32P, _I32P, _I32P,
@@ -148,6 +150,13 @@ def _host_i32(a):
     return arr, arr.ctypes.data_as(_I32P)
 
 
+def _same_length(*arrays):
+    """The C calls take one count per group of arrays: arrays given (not None) must agree."""
+    n = {int(a.shape[0]) for a in arrays if a is not None}
+    if len(n) > 1:
+        raise ValueError(f"array lengths differ: {sorted(n)}")
+
+
 def kv_desc(num_q_heads: int, num_kv_heads: int, pool_size: int, req_to_token,
             softmax_scale: Optional[float] = None, head_dim: int = 128) -> KVDesc:
     """Descriptor of the pool and of req_to_token (a [rows, stride] int32 CUDA tensor)."""
@@ -162,6 +171,10 @@ def kv_desc(num_q_heads: int, num_kv_heads: int, pool_size: int, req_to_token,
 
 def store_kv(desc: KVDesc, k_pool, v_pool, k_new, v_new, slots, stream=None):
     n = int(slots.shape[0]) if slots is not None else 0
+    row = desc.num_kv_heads * desc.head_dim
+    for name, t in (("k_new", k_new), ("v_new", v_new)):
+        if n > 0 and hasattr(t, "numel") and t.numel() != n * row:
+            raise ValueError(f"{name} holds {t.numel()} elements, slots ask for {n} x {row}")
     _check(lib().rx_store_kv(C.byref(desc), _ptr(k_pool), _ptr(v_pool), _ptr(k_new), _ptr(v_new),
                              _ptr(slots), n, _stream(stream)))
 
@@ -194,6 +207,12 @@ class Plan:
         _check(lib().rx_plan_workspace_size(self._h, C.byref(n)))
         return n.value
 
+    def launches(self) -> int:
+        """Kernels one attention call with the plan launches (rx_plan_launches)."""
+        n = np.zeros(1, np.int32)
+        _check(lib().rx_plan_launches(self._h, n.ctypes.data_as(_I32P)))
+        return int(n[0])
+
     def key_reads(self) -> int:
         """(key, KV head) rows of the pool the plan's kernels read (rx_plan_key_reads)."""
         n = np.zeros(1, np.int64)
@@ -216,6 +235,8 @@ def extend_plan(plan: Plan, desc: KVDesc, req_idx, prefix_len, extend_len, group
     gl, glp = _host_i32(group_prefix_len)
     pa, pap = _host_i32(group_parent)
     ng = 0 if gl is None else int(gl.shape[0])
+    _same_length(ri, pl, el, g)
+    _same_length(gl, pa)
     if pa is None:
         _check(lib().rx_extend_plan(plan.handle, C.byref(desc), int(ri.shape[0]), rip, plp, elp,
                                     gp_, ng, glp))
@@ -233,6 +254,8 @@ def decode_plan(plan: Plan, desc: KVDesc, req_idx, seq_len, group_of_req=None,
     gl, glp = _host_i32(group_prefix_len)
     pa, pap = _host_i32(group_parent)
     ng = 0 if gl is None else int(gl.shape[0])
+    _same_length(ri, sl, g)
+    _same_length(gl, pa)
     if pa is None:
         _check(lib().rx_decode_plan(plan.handle, C.byref(desc), int(ri.shape[0]), rip, slp, gp_,
                                     ng, glp))
@@ -433,6 +456,8 @@ def check_tables(req_to_token, pool_size: int, req_idx, key_len, group_of_req=No
     gl, glp = _host_i32(group_prefix_len)
     pa, pap = _host_i32(group_parent)
     ng = 0 if gl is None else int(gl.shape[0])
+    _same_length(ri, kl, g)
+    _same_length(gl, pa)
     bad = C.c_int64(-1)
     st = lib().rx_check_tables(t.ctypes.data_as(_I32P), int(t.shape[0]), int(t.shape[1]),
                                int(pool_size), int(ri.shape[0]), rip, klp, gp_, ng, glp, pap,

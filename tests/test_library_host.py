@@ -9,7 +9,7 @@ import numpy as np
 import pytest
 
 from oracle import accounting, radix as oradix
-from prefix_shared_kv_gb300 import rx
+from prefix_shared_kv_gb300 import rx, workloads as W
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 GOLDEN = os.path.join(ROOT, "tests", "golden")
@@ -149,7 +149,42 @@ def test_empty_batches_plan_to_no_work(librx):
     rx.extend_plan(p, d, [], [], [], [], [])
     assert p.workspace_size() == 256 and p.key_reads() == 0  # the header alone
     rx.decode_plan(p, d, [], [], [], [])
-    assert p.key_reads() == 0
+    assert p.key_reads() == 0 and p.launches() == 0
+
+
+def test_binding_rejects_arrays_of_different_lengths(librx):
+    p, d = rx.Plan(), _desc()
+    with pytest.raises(ValueError):
+        rx.extend_plan(p, d, [0], [10], [3], [])          # a group entry missing
+    with pytest.raises(ValueError):
+        rx.decode_plan(p, d, [0, 1], [5])                 # a length missing
+    with pytest.raises(ValueError):
+        rx.decode_plan(p, d, [0], [5], [0], [3, 4], [-1])  # a parent missing
+
+
+def test_plan_launch_counts(librx):
+    """What rx_plan_launches reports: one tensor-core launch for extend work; for decode, the
+    tensor-core kernel only when a shared-prefix unit stacks >= 32 query rows per KV head, the
+    mma.sync kernel for the rest, and the merge."""
+    d = _desc(rows=40, stride=4096, hq=8, hkv=2)  # 4 query heads per KV head
+    p = rx.Plan()
+    rx.extend_plan(p, d, [0, 1], [100, 100], [10, 10], [0, 0], [100])
+    assert p.launches() == 1
+    rx.extend_plan(p, d, [0], [100], [0])  # nothing to extend
+    assert p.launches() == 0
+    rx.decode_plan(p, d, list(range(4)), [300] * 4, [0] * 4, [200])  # 16 rows: mma.sync only
+    assert p.launches() == 2
+    rx.decode_plan(p, d, list(range(8)), [200] * 8, [0] * 8, [200])  # 32 rows, no own keys
+    assert p.launches() == 2
+    rx.decode_plan(p, d, list(range(8)), [300] * 8, [0] * 8, [200])  # 32 rows and own keys
+    assert p.launches() == 3
+    wl = W.NAMED["radix-mixed"]()
+    dc = wl.steps[0].decode
+    dd = _desc(rows=wl.req_to_token.shape[0], stride=wl.req_to_token.shape[1],
+               hq=wl.num_q_heads, hkv=wl.num_kv_heads, pool=wl.pool_size)
+    rx.decode_plan(p, dd, dc.req_idx, dc.seq_len, dc.group_of_req, dc.group_prefix_len,
+                   dc.group_parent)
+    assert p.launches() == 3
 
 
 def test_tree_plan_argument_checks(librx):
