@@ -17,6 +17,7 @@
 #include <cuda_runtime.h>
 #include <math_constants.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "ptx.cuh"
@@ -332,13 +333,18 @@ std::mutex g_aux_lock;
 int launch_decode(const rx_kv_desc* d, const PlanHeader* h, const void* k_pool,
                   const void* v_pool, const void* q, void* o, float* lse, void* ws,
                   void* stream) {
-  static bool attr_set = false;
-  if (!attr_set) {
+  // kernel attributes belong to the current device: set once per device (bit d of the mask)
+  static std::atomic<uint64_t> attr_set{0};
+  int cur = 0;
+  cudaError_t de = cudaGetDevice(&cur);
+  if (de != cudaSuccess) return (int)de;
+  if (cur < 0 || cur >= kMaxDevices) return (int)cudaErrorInvalidDevice;
+  if (!((attr_set.load() >> cur) & 1)) {
     cudaError_t e = cudaFuncSetAttribute(decode_partial_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kDecSmemBytes);
     if (e != cudaSuccess) return (int)e;
-    attr_set = true;
+    attr_set.fetch_or(1ull << cur);
   }
   uint8_t* base = static_cast<uint8_t*>(ws);
   DecParams p;

@@ -43,6 +43,8 @@
 #include <cuda_runtime.h>
 #include <math_constants.h>
 
+#include <atomic>
+
 #include "ptx.cuh"
 #include "rx_internal.h"
 #include "tc.cuh"
@@ -800,8 +802,13 @@ int launch_attn_items(const rx_kv_desc* d, const ExtItem* items, const ExtRow* r
                       const ExtSeg* segs, int32_t n_items, const void* k_pool, const void* v_pool,
                       const void* q, void* o, float* lse, float* part_o, float* part_lse,
                       int32_t* status, void* stream) {
-  static bool attr_set = false;
-  if (!attr_set) {
+  // kernel attributes belong to the current device: set once per device (bit d of the mask)
+  static std::atomic<uint64_t> attr_set{0};
+  int dev = 0;
+  cudaError_t de = cudaGetDevice(&dev);
+  if (de != cudaSuccess) return (int)de;
+  if (dev < 0 || dev >= 64) return (int)cudaErrorInvalidDevice;
+  if (!((attr_set.load() >> dev) & 1)) {
     // The softmax warpgroups raise their register budget with what the other warpgroups give up;
     // that only balances when every thread starts with exactly kRegsLaunch registers (with fewer,
     // the raise would wait for registers that never come), so any other build is refused.
@@ -812,7 +819,7 @@ int launch_attn_items(const rx_kv_desc* d, const ExtItem* items, const ExtRow* r
     e = cudaFuncSetAttribute(extend_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kSmem);
     if (e != cudaSuccess) return (int)e;
-    attr_set = true;
+    attr_set.fetch_or(1ull << dev);
   }
   if (n_items == 0) return 0;
   ExtParams p;
@@ -842,9 +849,8 @@ int launch_attn_items(const rx_kv_desc* d, const ExtItem* items, const ExtRow* r
   p.n_items = n_items;
   p.o32 = (reinterpret_cast<uintptr_t>(o) & 31u) == 0;
   // one persistent CTA per SM (a CTA fills an SM's shared memory), at most one per item
-  int dev = 0, n_sm = 0;
-  cudaError_t ce = cudaGetDevice(&dev);
-  if (ce == cudaSuccess) ce = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
+  int n_sm = 0;
+  const cudaError_t ce = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
   if (ce != cudaSuccess) return (int)ce;
   const int grid = n_items < n_sm ? n_items : n_sm;
   extend_tc_kernel<<<grid, kThreads, kSmem, (cudaStream_t)stream>>>(p, k_map, v_map);

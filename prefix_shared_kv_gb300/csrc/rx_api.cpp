@@ -3,6 +3,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -62,18 +63,21 @@ rx_status check_desc(const rx_kv_desc* d, bool need_table) {
   return RX_OK;
 }
 
+// SMs of the current device (plans are sized for it); 152 when no device can be asked
 int device_sms() {
-  static int cached = 0;
-  if (cached) return cached;
+  static std::atomic<int> cached[64];
   int dev = 0, n = 0;
-  if (cudaGetDevice(&dev) == cudaSuccess &&
-      cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && n > 0) {
-    cached = n;
-  } else {
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
     cudaGetLastError();
-    n = 152;
+    return 152;
   }
-  return n;
+  if ((n = cached[dev].load()) > 0) return n;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && n > 0) {
+    cached[dev].store(n);
+    return n;
+  }
+  cudaGetLastError();
+  return 152;
 }
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
