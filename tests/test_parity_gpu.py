@@ -204,6 +204,42 @@ def test_unit_values_give_unit_output(cuda, kind):
             _within_one_ulp_of_one(dw.steps[i].dec_o, f"{kind} decode")
 
 
+def test_cuda_graph_replay_of_a_step(cuda):
+    """A whole step -- store, extend, and a decode whose tensor-core and mma.sync units run on
+    two streams (fork and join through events) before the merge -- captured once into a CUDA
+    graph after a first eager run, then replayed: the results match the oracle, and a second
+    replay gives the same bits as the first."""
+    wl = W.tree_workload(41, 8, 8, depth=2, fanout=3, seg_lo=50, seg_hi=300, p_empty=0.0,
+                         n_decode=40, tail_hi=40, n_extend=6, own_hi=30, ext_lo=1, ext_hi=100)
+    dw = DeviceWorkload(wl, cuda)
+    ds = dw.steps[0]
+    assert ds.dec_plan.launches() == 3 and ds.ext_plan.launches() == 1
+    dw.run_step(0)  # the first calls set kernel attributes and create the second stream
+    torch.cuda.synchronize()
+    eager = [t.clone() for t in (ds.ext_o, ds.ext_lse, ds.dec_o, ds.dec_lse)]
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        dw.run_step(0)
+    outs = (ds.ext_o, ds.ext_lse, ds.dec_o, ds.dec_lse)
+    replays = []
+    for _ in range(2):
+        for t in outs:
+            t.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        replays.append([t.clone() for t in outs])
+    kp, vp = oracle_pools(wl, 0)
+    st = wl.steps[0]
+    e, d = st.extend, st.decode
+    o, l = A.extend(e.q, kp, vp, wl.req_to_token, e.req_idx, e.prefix_len, e.extend_len, e.cu_q,
+                    wl.softmax_scale)
+    assert_close(replays[0][0], replays[0][1], o, l, what="graph extend")
+    o, l = A.decode(d.q, kp, vp, wl.req_to_token, d.req_idx, d.seq_len, wl.softmax_scale)
+    assert_close(replays[0][2], replays[0][3], o, l, what="graph decode")
+    for a, b, c in zip(replays[0], replays[1], eager):
+        assert torch.equal(a, b) and torch.equal(a, c)
+
+
 # ---------------------------------------------------------------------------------------------
 # Decode: groups of many members, single-member groups, empty own parts, long prefixes.
 # ---------------------------------------------------------------------------------------------
