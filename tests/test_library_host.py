@@ -128,6 +128,25 @@ def test_plan_argument_checks(librx):
         rx.Plan().workspace_size()
 
 
+def test_size_limits_are_refused_on_the_host(librx):
+    """Limits of the int32 tables, refused by the planners before any row is built (planning only:
+    no attention call is made with these descriptors)."""
+    p = rx.Plan()
+    big = _desc(rows=2, stride=1 << 30)
+    with pytest.raises(rx.RxError) as e:  # 2^31 new rows in one batch
+        rx.extend_plan(p, big, [0, 1], [0, 0], [1 << 30, 1 << 30])
+    assert e.value.status == rx.RX_ERR_RANGE
+    with pytest.raises(rx.RxError) as e:  # a pool of 2^31 slots
+        rx.decode_plan(p, _desc(pool=1 << 31), [0], [1])
+    assert e.value.status == rx.RX_ERR_INVALID
+    with pytest.raises(rx.RxError) as e:  # a decode request must attend to its own token
+        rx.decode_plan(p, _desc(), [0], [0])
+    assert e.value.status in (rx.RX_ERR_INVALID, rx.RX_ERR_RANGE)
+    with pytest.raises(rx.RxError) as e:  # more than 256 KV heads
+        rx.decode_plan(p, _desc(hq=512, hkv=512), [0], [1])
+    assert e.value.status == rx.RX_ERR_UNSUPPORTED
+
+
 def test_plans_size_workspaces_without_a_gpu(librx):
     p = rx.Plan()
     d = _desc(rows=8, stride=4096, hq=32, hkv=8)
