@@ -301,3 +301,50 @@ def test_block_granular_match_reuses_whole_pages(librx):
         saved, got = t.match(e.tokens[r], match_unit=16)
         assert saved == 992 and np.array_equal(got, slots)
         assert np.all(got.reshape(-1, 16) // 16 == (got.reshape(-1, 16) // 16)[:, :1])  # pages
+
+
+def _has_gpu():
+    try:
+        import torch
+        return torch.cuda.is_available()
+    except Exception:
+        return False
+
+
+@pytest.mark.skipif(_has_gpu(), reason="fake device addresses: run where no GPU could be reached")
+def test_attention_and_store_refuse_bad_pointers_before_any_launch(librx):
+    """Host-side checks of the calls that launch kernels: each call below carries exactly one
+    defect (a NULL or misaligned tensor, a missing, misaligned or short workspace, a plan of the
+    other kind, a descriptor the plan was not built with) and must return its code before anything
+    is enqueued.  The addresses are fake and never dereferenced."""
+    import ctypes as C
+    d = _desc(rows=4, stride=64, hq=8, hkv=2)
+    p = rx.Plan()
+    rx.extend_plan(p, d, [0], [10], [5])
+    nb = p.workspace_size()
+    good = dict(k=0x10000, v=0x20000, q=0x30000, o=0x40000, lse=0x50000, ws=0x100000, nb=nb)
+
+    def call(fn, desc=d, **bad):
+        assert len(bad) == 1  # never a call without a defect: that one would launch
+        a = dict(good, **bad)
+        return fn(p.handle, C.byref(desc), a["k"], a["v"], a["q"], a["o"], a["lse"], a["ws"],
+                  a["nb"], None)
+
+    ext, dec = librx.rx_extend_attn, librx.rx_decode_attn
+    assert call(ext, q=0) == rx.RX_ERR_INVALID
+    assert call(ext, k=0x10008) == rx.RX_ERR_INVALID
+    assert call(ext, o=0x40008) == rx.RX_ERR_INVALID
+    assert call(ext, lse=0x50004) == rx.RX_ERR_INVALID
+    assert call(ext, ws=0) == rx.RX_ERR_WORKSPACE
+    assert call(ext, ws=0x100010) == rx.RX_ERR_INVALID
+    assert call(ext, nb=nb - 1) == rx.RX_ERR_WORKSPACE
+    assert call(dec, q=0) == rx.RX_ERR_INVALID
+    assert call(ext, desc=_desc(rows=4, stride=64, hq=8, hkv=2, pool=256),
+                q=0x30000) == rx.RX_ERR_INVALID  # plan built for another pool size
+    # the plan is an extend plan: the decode call refuses it whatever the pointers
+    assert dec(p.handle, C.byref(d), 0x10000, 0x20000, 0x30000, 0x40000, 0x50000, 0x100000, nb,
+               None) == rx.RX_ERR_INVALID
+    st = librx.rx_store_kv
+    assert st(C.byref(d), 0x10000, 0x20000, 0x60008, 0x70000, 0x80000, 3, None) == rx.RX_ERR_INVALID
+    assert st(C.byref(d), 0x10000, 0x20000, 0x60000, 0x70000, None, 3, None) == rx.RX_ERR_INVALID
+    assert st(C.byref(d), 0x10000, 0x20000, 0x60000, 0x70000, 0x80000, -1, None) == rx.RX_ERR_INVALID

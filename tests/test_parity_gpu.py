@@ -240,6 +240,42 @@ def test_cuda_graph_replay_of_a_step(cuda):
         assert torch.equal(a, b) and torch.equal(a, c)
 
 
+def test_kernels_write_nothing_outside_their_outputs(cuda):
+    """o and lse of both calls sit in buffers with 4,096 guard elements on each side, filled
+    with a pattern: after a step (extend; decode with tensor-core units, mma.sync units and the
+    merge) the guards are unchanged, and the outputs equal those of a run in plain buffers."""
+    def make():
+        return W.tree_workload(41, 8, 8, depth=2, fanout=3, seg_lo=50, seg_hi=300, p_empty=0.0,
+                               n_decode=40, tail_hi=40, n_extend=6, own_hi=30, ext_lo=1,
+                               ext_hi=100)
+    plain = DeviceWorkload(make(), cuda)
+    plain.run_step(0)
+    dw = DeviceWorkload(make(), cuda)
+    ds = dw.steps[0]
+    assert ds.dec_plan.launches() == 3
+    G = 4096
+    guards = []
+
+    def guarded(t):
+        as_int = torch.int16 if t.element_size() == 2 else torch.int32
+        pattern = 0x7FC1 if t.element_size() == 2 else 0x7F8A5A5A
+        buf = torch.empty(t.numel() + 2 * G, dtype=t.dtype, device=cuda)
+        buf.view(as_int).fill_(pattern)
+        guards.append((buf.view(as_int), pattern))
+        return buf[G:G + t.numel()].view(t.shape)
+
+    ds.ext_o, ds.ext_lse = guarded(ds.ext_o), guarded(ds.ext_lse)
+    ds.dec_o, ds.dec_lse = guarded(ds.dec_o), guarded(ds.dec_lse)
+    dw.run_step(0)
+    torch.cuda.synchronize()
+    for b, pattern in guards:
+        assert bool((b[:G] == pattern).all()) and bool((b[-G:] == pattern).all())
+    p = plain.steps[0]
+    for a, b in ((ds.ext_o, p.ext_o), (ds.ext_lse, p.ext_lse), (ds.dec_o, p.dec_o),
+                 (ds.dec_lse, p.dec_lse)):
+        assert torch.equal(a, b)
+
+
 # ---------------------------------------------------------------------------------------------
 # Decode: groups of many members, single-member groups, empty own parts, long prefixes.
 # ---------------------------------------------------------------------------------------------
