@@ -12,9 +12,10 @@ time of the whole step (store + extend + decode), in TFLOP/s; `parts` gives each
 own roofline (decode: unique KV bytes / time vs HBM; extend: FLOPs / time vs bf16 tensor peak;
 store: bytes moved / time).  Decode-only workloads report decode GB/s instead.
 
-Timing: W warm-up steps, then K steps, each bracketed by CUDA events on the launch stream with a
-256 MiB L2 flush between steps (outside the events); barrier + synchronize on both sides; max over
-ranks.  `--impl reference` times the fp64 oracle on host cores on a bounded sample instead.
+Timing: W warm-up steps, then K steps, each bracketed by CUDA events on the launch stream with an
+L2 flush between steps (outside the events: a 256 MiB buffer written, then another read, so no
+dirty flush lines are left for the step to write back); barrier + synchronize on both sides; max
+over ranks.  `--impl reference` times the fp64 oracle on host cores on a bounded sample instead.
 """
 from __future__ import annotations
 
@@ -314,7 +315,15 @@ def main():
     peaks, peak_src = load_peaks()
     dw = DeviceWorkload(wl, dev)
     stream = torch.cuda.current_stream(dev)
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    # L2 flush between steps, outside the timed region: write a 256 MiB buffer (twice the L2), then
+    # read another one, so that the written lines are back in DRAM before the next step starts
+    # (left dirty in L2, their write-back would be timed inside the step's first kernel)
+    flush_w = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    flush_r = torch.zeros(256 << 20, dtype=torch.uint8, device=dev)
+
+    def flush_l2():
+        flush_w.zero_()
+        flush_r.max()
 
     parts = [("store", dw.store), ("extend", dw.extend), ("decode", dw.decode)]
     if args.only:
@@ -325,7 +334,7 @@ def main():
             f(0)
 
     for _ in range(max(args.warmup, 0)):
-        flush.zero_()
+        flush_l2()
         step()
     torch.cuda.synchronize(dev)
     barrier(pg, dev)
@@ -336,7 +345,7 @@ def main():
     clocks.start()
     t_wall = time.perf_counter()
     for k in range(args.steps):
-        flush.zero_()
+        flush_l2()
         ev[k][0].record(stream)
         for j, (_, f) in enumerate(parts):
             f(0)
@@ -425,7 +434,8 @@ def main():
                 "dtype": "bf16", "data": "synthetic",
                 "config": {"workload": wl.name, "recipe": wl.recipe,
                            "parallelism": f"replicas x{world}",
-                           "l2": "256 MiB buffer written between timed steps"},
+                           "l2": "between timed steps a 256 MiB buffer written, then another "
+                                 "256 MiB buffer read (outside the timed region)"},
                 "parts": pdesc, "roofline": roof, "gpu_launches": gpu_launches,
                 "clocks": clk, "e2e": e2e, "cpu_baseline": cpu, "wall_timed_s": t_wall}
         if args.only:
