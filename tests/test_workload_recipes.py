@@ -1,0 +1,129 @@
+"""The benchmark's named workloads have the shapes their recipes state (head counts, request
+counts, prefix / extend / distinct lengths, shared-prefix structure, pool slots), and the work the
+benchmark divides by (extend FLOPs over unmasked pairs, unique decode KV bytes, store bytes) is
+what those shapes give.  Host only."""
+import os
+import sys
+
+import numpy as np
+import pytest
+
+from prefix_shared_kv_gb300 import workloads as W
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+
+
+def rows_share(table, rows, n):
+    """All the given table rows hold the same first n slots."""
+    return all(np.array_equal(table[rows[0], :n], table[r, :n]) for r in rows[1:])
+
+
+def distinct_tokens_have_distinct_slots(wl):
+    """Every slot is one token: a slot that appears in two rows appears at the same position of
+    both (a shared prefix), never as two different tokens; and every slot is inside the pool."""
+    lengths = {}
+    for st in wl.steps:
+        for b in (st.extend, st.decode):
+            if b is None:
+                continue
+            n = (b.prefix_len + b.extend_len) if b is st.extend else b.seq_len
+            for r, k in zip(b.req_idx, n):
+                lengths[int(r)] = max(lengths.get(int(r), 0), int(k))
+    slots = np.concatenate([wl.req_to_token[r, :k] for r, k in lengths.items()]).astype(np.int64)
+    pos = np.concatenate([np.arange(k) for k in lengths.values()]).astype(np.int64)
+    assert slots.min() >= 0 and slots.max() < wl.pool_size
+    pairs = np.unique(slots * (1 << 32) + pos)  # distinct (slot, position) pairs
+    assert np.unique(pairs >> 32).size == pairs.size  # each slot at one position only
+    return True
+
+
+def test_tiny():
+    wl = W.tiny()
+    assert (wl.num_q_heads, wl.num_kv_heads, wl.pool_size) == (8, 2, 4096)
+    e = wl.steps[0].extend
+    assert list(e.prefix_len) == [1000] * 4 and list(e.extend_len) == [40] * 4
+    assert rows_share(wl.req_to_token, list(e.req_idx), 1000)
+    assert [list(st.decode.seq_len) for st in wl.steps[1:]] == [[1041 + s] * 4 for s in range(8)]
+    used = {int(s) for st in wl.steps for s in st.store_slots} | set(
+        int(s) for s in wl.req_to_token[e.req_idx[0], :1000])
+    assert len(used) == 1192 and distinct_tokens_have_distinct_slots(wl)
+
+
+def test_extend_workload():
+    wl = W.NAMED["extend"]()
+    e = wl.steps[0].extend
+    assert (wl.num_q_heads, wl.num_kv_heads) == (32, 32) and len(e.req_idx) == 64
+    assert (e.prefix_len == 2000).all() and e.extend_len.min() >= 40 and e.extend_len.max() <= 200
+    for g in range(4):
+        assert rows_share(wl.req_to_token, list(e.req_idx[e.group_of_req == g]), 2000)
+    assert distinct_tokens_have_distinct_slots(wl)
+    w = bench.work_counts(wl)
+    pairs = float(np.sum(e.extend_len * 2000.0 + e.extend_len * (e.extend_len + 1) / 2.0))
+    assert w["extend_flops"] == pytest.approx(4 * 128 * 32 * pairs)
+    assert w["extend_flops"] == pytest.approx(2.604e11, rel=0.1)  # E ~ U[40, 200], mean 120
+
+
+@pytest.mark.parametrize("name,hkv,prefix,lo,hi,tokens", [
+    ("decode", 32, 2000, 100, 500, 108800),
+    ("gqa-decode", 8, 16000, 200, 1000, 409600)])
+def test_decode_workloads(name, hkv, prefix, lo, hi, tokens):
+    wl = W.NAMED[name]()
+    d = wl.steps[0].decode
+    assert (wl.num_q_heads, wl.num_kv_heads) == (32, hkv) and len(d.req_idx) == 256
+    own = d.seq_len - prefix
+    assert own.min() >= lo and own.max() <= hi
+    for g in range(16):
+        assert (d.group_of_req == g).sum() == 16
+        assert rows_share(wl.req_to_token, list(d.req_idx[d.group_of_req == g]), prefix)
+    if name == "gqa-decode":
+        assert wl.pool_size >= 409600
+    assert distinct_tokens_have_distinct_slots(wl)
+    w = bench.work_counts(wl)
+    unique = 16 * prefix + int(own.sum())
+    assert w["decode_kv_bytes"] == unique * hkv * 128 * 2 * 2
+    assert unique == pytest.approx(tokens, rel=0.05)
+
+
+def test_radix_mixed():
+    wl = W.NAMED["radix-mixed"]()
+    st = wl.steps[0]
+    e, d = st.extend, st.decode
+    assert (wl.num_q_heads, wl.num_kv_heads, wl.pool_size) == (32, 32, 32768)
+    assert sorted(zip(e.prefix_len.tolist(), e.extend_len.tolist())) == \
+        [(0, 1500)] * 8 + [(1700, 64)] * 16
+    assert len(d.req_idx) == 40 and (d.seq_len - 1700).min() >= 1 and (d.seq_len - 1700).max() <= 32
+    assert len(st.store_slots) == 16 * 64 + 8 * 1500 + 40
+    # the tree: the 1000-token system prompt under every hit, a 500-token branch under four
+    # leaves, a 200-token leaf under its requests
+    hits = list(e.req_idx[e.prefix_len > 0]) + list(d.req_idx)
+    assert rows_share(wl.req_to_token, hits, 1000)
+    par, gpl = d.group_parent, d.group_prefix_len
+    assert list(gpl[:1]) == [1000] and (gpl[1:9] == 1500).all() and (gpl[9:] == 1700).all()
+    for leaf in range(9, 41):
+        assert par[leaf] == 1 + (leaf - 9) // 4
+        members = list(d.req_idx[d.group_of_req == leaf])
+        assert rows_share(wl.req_to_token, members, 1700)
+    assert distinct_tokens_have_distinct_slots(wl)
+    w = bench.work_counts(wl)
+    assert w["extend_flops"] == 4 * 128 * 32 * 10780080  # unmasked pairs, exactly
+    tails = int((d.seq_len - 1700).sum())
+    # tree-unique decode KV: 1,000 + 8 x 500 + the 32 leaves' 200 (every leaf has a request:
+    # requests j and j + 32 share leaf j) + each request's own tail
+    assert w["decode_kv_bytes"] == (1000 + 8 * 500 + 32 * 200 + tails) * 32 * 512
+    assert w["store_bytes"] == 13064 * 32 * 256 * 2 * 2
+
+
+def test_chunked_prefill():
+    wl = W.NAMED["chunked-prefill"]()
+    assert (wl.num_q_heads, wl.num_kv_heads) == (32, 8) and len(wl.steps) == 3
+    for i, st in enumerate(wl.steps):
+        e, d = st.extend, st.decode
+        assert list(e.extend_len) == [2048] and list(e.prefix_len) == [1024 + 2048 * i]
+        assert len(d.req_idx) == 64
+        own = d.seq_len - 1024 - i - 1  # own cached tail: U[200, 1000], one new token a step
+        assert own.min() >= 200 and own.max() <= 1000
+        if i:
+            assert (own == wl.steps[0].decode.seq_len - 1024 - 1).all()
+    assert distinct_tokens_have_distinct_slots(wl)
