@@ -422,7 +422,7 @@ def main():
         e2e = run_e2e(wl, dw, dev, args, pg, world, w, unit, scale, has_ext)
 
     cpu = None
-    if rank == 0 and not args.no_cpu_baseline and not args.only:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.only:  # N = 1 only
         er, dr, est, sample, threads = oracle_sample_rate(wl, budget_s=12.0)
         cpu = {"value": er if has_ext else dr, "unit": unit, "cores": threads, "kind": "oracle",
                "sample": sample}
