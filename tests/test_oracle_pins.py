@@ -83,6 +83,21 @@ def test_decode_matches_brute_force():
             assert abs(lse[b, h] - bl) < 1e-12
 
 
+def test_decode_is_an_extend_of_its_current_token():
+    """Store-then-attend: a decode step is the extend of one new token (the current one) over a
+    cached prefix of seq_len - 1 keys, so the two oracle functions agree on every request."""
+    wl = W.decode_workload(5, 8, 2, n_groups=2, members=4, prefix=40, dist_lo=1, dist_hi=30,
+                           ungrouped=2)
+    kp, vp = _stored_pools(wl)
+    d = wl.steps[0].decode
+    B = len(d.req_idx)
+    o, lse = A.decode(d.q, kp, vp, wl.req_to_token, d.req_idx, d.seq_len, wl.softmax_scale)
+    oe, le = A.extend(d.q, kp, vp, wl.req_to_token, d.req_idx, d.seq_len - 1,
+                      np.ones(B, np.int32), np.arange(B + 1, dtype=np.int32), wl.softmax_scale)
+    np.testing.assert_allclose(oe, o, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(le, lse, rtol=0, atol=1e-12)
+
+
 # ---------------------------------------------------------------------------------------------
 # Closed forms of the softmax definition.
 # ---------------------------------------------------------------------------------------------
