@@ -101,6 +101,11 @@ void rx_plan_destroy(rx_plan* plan);
  * a decode plan launches up to three: tensor-core shared-prefix units, mma.sync units, merge).
  * For a caller's and a benchmark's bookkeeping; (host). */
 rx_status rx_plan_launches(const rx_plan* plan, int32_t* launches);
+/* Rows of q / o / lse an attention call with the built plan reads and writes: the sum of
+ * extend_len for an extend plan, the batch for a decode plan.  The calls take raw pointers and
+ * cannot see the buffers' sizes: a caller checks its tensors against this (the Python binding
+ * does, before every call).  (host) */
+rx_status rx_plan_rows(const rx_plan* plan, int64_t* rows);
 /* Bytes of device workspace the built plan needs (tables + partial results). */
 rx_status rx_plan_workspace_size(const rx_plan* plan, size_t* bytes);
 /* Copy the plan's tables into `workspace` (device, >= rx_plan_workspace_size bytes, 256-byte

@@ -232,6 +232,14 @@ rx_status rx_plan_key_reads(const rx_plan* plan, int64_t* rows) {
   return RX_OK;
 }
 
+rx_status rx_plan_rows(const rx_plan* plan, int64_t* rows) {
+  if (!plan || !rows) return fail(RX_ERR_INVALID, "NULL argument");
+  if (!plan->kind) return fail(RX_ERR_INVALID, "plan has not been built");
+  const PlanHeader h = plan->hdr();
+  *rows = plan->kind == 1 ? h.n_rows : h.batch;  // extend: one row per new token
+  return RX_OK;
+}
+
 rx_status rx_plan_launches(const rx_plan* plan, int32_t* launches) {
   if (!plan || !launches) return fail(RX_ERR_INVALID, "NULL argument");
   if (!plan->kind) return fail(RX_ERR_INVALID, "plan has not been built");

@@ -22,6 +22,7 @@ RX_OK, RX_ERR_INVALID, RX_ERR_RANGE, RX_ERR_UNSUPPORTED, RX_ERR_CUDA, RX_ERR_TIM
 EXPORTED = [
     "rx_status_string", "rx_last_error", "rx_store_kv", "rx_plan_create", "rx_plan_destroy",
     "rx_plan_workspace_size", "rx_plan_upload", "rx_plan_key_reads", "rx_plan_launches",
+    "rx_plan_rows",
     "rx_extend_plan",
     "rx_extend_plan_tree", "rx_extend_attn", "rx_decode_plan", "rx_decode_plan_tree",
     "rx_decode_attn", "rx_decode_attn_noalloc", "rx_read_status", "rx_selftest_wait_timeout",
@@ -71,6 +72,7 @@ def lib():
         "rx_plan_upload": (C.c_int, [_P, _P, C.c_size_t, _P]),
         "rx_plan_key_reads": (C.c_int, [_P, _I64P]),
         "rx_plan_launches": (C.c_int, [_P, _I32P]),
+        "rx_plan_rows": (C.c_int, [_P, _I64P]),
         "rx_extend_plan": (C.c_int, [_P, C.POINTER(KVDesc), C.c_int32, _I32P, _I32P, _I32P,
                                      _I32P, C.c_int32, _I32P]),
         "rx_extend_plan_tree": (C.c_int, [_P, C.POINTER(KVDesc), C.c_int32, _I32P, _I32P, _I32P,
@@ -207,6 +209,12 @@ class Plan:
         _check(lib().rx_plan_workspace_size(self._h, C.byref(n)))
         return n.value
 
+    def rows(self) -> int:
+        """Rows of q / o / lse an attention call with the plan touches (rx_plan_rows)."""
+        n = np.zeros(1, np.int64)
+        _check(lib().rx_plan_rows(self._h, n.ctypes.data_as(_I64P)))
+        return int(n[0])
+
     def launches(self) -> int:
         """Kernels one attention call with the plan launches (rx_plan_launches)."""
         n = np.zeros(1, np.int32)
@@ -270,13 +278,30 @@ def _nbytes(t) -> int:
     return t.numel() * t.element_size()
 
 
+def check_io(plan: Plan, desc: KVDesc, q, o, lse):
+    """The kernels write o and lse by row index, so buffers smaller than the plan's rows would be
+    written past their end: tensors (anything with numel / dtype) must hold exactly the plan's
+    rows -- q, o bf16 [rows, Hq, head_dim], lse float32 [rows, Hq].  Raw addresses (ints) are
+    the caller's responsibility."""
+    n = plan.rows()
+    per = desc.num_q_heads * desc.head_dim
+    for name, t, want, dt in (("q", q, n * per, "bfloat16"), ("o", o, n * per, "bfloat16"),
+                              ("lse", lse, n * desc.num_q_heads, "float32")):
+        if hasattr(t, "numel") and t.numel() != want:
+            raise ValueError(f"{name} holds {t.numel()} elements; the plan's {n} rows need {want}")
+        if hasattr(t, "dtype") and not str(t.dtype).endswith(dt):
+            raise ValueError(f"{name} is {t.dtype}, {dt} expected")
+
+
 def extend_attn(plan: Plan, desc: KVDesc, k_pool, v_pool, q, o, lse, workspace, stream=None):
+    check_io(plan, desc, q, o, lse)
     _check(lib().rx_extend_attn(plan.handle, C.byref(desc), _ptr(k_pool), _ptr(v_pool), _ptr(q),
                                 _ptr(o), _ptr(lse), _ptr(workspace), _nbytes(workspace),
                                 _stream(stream)))
 
 
 def decode_attn(plan: Plan, desc: KVDesc, k_pool, v_pool, q, o, lse, workspace, stream=None):
+    check_io(plan, desc, q, o, lse)
     _check(lib().rx_decode_attn(plan.handle, C.byref(desc), _ptr(k_pool), _ptr(v_pool), _ptr(q),
                                 _ptr(o), _ptr(lse), _ptr(workspace), _nbytes(workspace),
                                 _stream(stream)))
@@ -284,6 +309,7 @@ def decode_attn(plan: Plan, desc: KVDesc, k_pool, v_pool, q, o, lse, workspace, 
 
 def decode_attn_noalloc(plan: Plan, desc: KVDesc, k_pool, v_pool, q, o, lse, stream=None):
     """rx_decode_attn_noalloc: decode without a workspace (the library's own scratch is used)."""
+    check_io(plan, desc, q, o, lse)
     _check(lib().rx_decode_attn_noalloc(plan.handle, C.byref(desc), _ptr(k_pool), _ptr(v_pool),
                                         _ptr(q), _ptr(o), _ptr(lse), _stream(stream)))
 

@@ -348,3 +348,44 @@ def test_attention_and_store_refuse_bad_pointers_before_any_launch(librx):
     assert st(C.byref(d), 0x10000, 0x20000, 0x60008, 0x70000, 0x80000, 3, None) == rx.RX_ERR_INVALID
     assert st(C.byref(d), 0x10000, 0x20000, 0x60000, 0x70000, None, 3, None) == rx.RX_ERR_INVALID
     assert st(C.byref(d), 0x10000, 0x20000, 0x60000, 0x70000, 0x80000, -1, None) == rx.RX_ERR_INVALID
+
+
+def test_plan_rows_and_the_bindings_size_checks(librx):
+    """rx_plan_rows is the q / o / lse row count a call touches (the sum of extend_len; the
+    batch); the binding refuses tensors of another size or dtype before calling in (meta tensors:
+    shapes and dtypes only, nothing that could reach a device)."""
+    import torch
+    for wl in (W.tiny(), W.extend_workload(2, 8, 2, n_groups=2, members=3, prefix=50, ext_lo=0,
+                                           ext_hi=20, ungrouped=2, ungrouped_prefix=5),
+               W.tree_workload(3, 8, 8, depth=2, fanout=2, seg_lo=0, seg_hi=40, p_empty=0.3,
+                               n_decode=9, tail_hi=5, n_extend=4, own_hi=6, ext_lo=1, ext_hi=9)):
+        d = _desc(rows=wl.req_to_token.shape[0], stride=wl.req_to_token.shape[1],
+                  hq=wl.num_q_heads, hkv=wl.num_kv_heads, pool=wl.pool_size)
+        for st in wl.steps:
+            for b in (st.extend, st.decode):
+                if b is None:
+                    continue
+                p = rx.Plan()
+                if b is st.extend:
+                    rx.extend_plan(p, d, b.req_idx, b.prefix_len, b.extend_len, b.group_of_req,
+                                   b.group_prefix_len, b.group_parent)
+                    n = int(b.extend_len.sum())
+                else:
+                    rx.decode_plan(p, d, b.req_idx, b.seq_len, b.group_of_req,
+                                   b.group_prefix_len, b.group_parent)
+                    n = len(b.req_idx)
+                assert p.rows() == n
+                hq = wl.num_q_heads
+                q = torch.empty((n, hq, 128), dtype=torch.bfloat16, device="meta")
+                lse = torch.empty((n, hq), dtype=torch.float32, device="meta")
+                rx.check_io(p, d, q, q, lse)  # exact: accepted
+                with pytest.raises(ValueError):
+                    rx.check_io(p, d, q, torch.empty((n + 1, hq, 128), dtype=torch.bfloat16,
+                                                     device="meta"), lse)
+                with pytest.raises(ValueError):
+                    rx.check_io(p, d, q, q, torch.empty((n, hq), dtype=torch.bfloat16,
+                                                        device="meta"))
+    p = rx.Plan()
+    rx.decode_plan(p, _desc(), [], [])
+    assert p.rows() == 0
+    rx.check_io(p, _desc(), None, None, None)  # an empty batch may pass no tensors
