@@ -116,15 +116,20 @@ class Builder:
     page order, its last page possibly part-filled (block-granular pools)."""
 
     def __init__(self, rng: np.random.Generator, num_q_heads: int, num_kv_heads: int,
-                 pool_size: int, head_dim: int = HEAD_DIM, page: int = 1):
+                 pool_size: int, head_dim: int = HEAD_DIM, page: int = 1, values: bool = True):
+        # values=False: the same draws in the same order (so the same slots, lengths, tokens and
+        # new tokens' KV), but the cached KV is not written into pools (structure-only checks of
+        # full-size workloads, without allocating their pools)
+        self.values = values
         self.rng = rng
         self.hq, self.hkv, self.d = num_q_heads, num_kv_heads, head_dim
         self.pool_size = pool_size
         self.page = page
         self.perm = rng.permutation(pool_size // page).astype(np.int32)
         self.next = 0
-        self.k_pool = np.zeros((pool_size, num_kv_heads, head_dim), dtype=np.uint16)
-        self.v_pool = np.zeros((pool_size, num_kv_heads, head_dim), dtype=np.uint16)
+        pool_rows = pool_size if values else 0
+        self.k_pool = np.zeros((pool_rows, num_kv_heads, head_dim), dtype=np.uint16)
+        self.v_pool = np.zeros((pool_rows, num_kv_heads, head_dim), dtype=np.uint16)
         self.rows: List[np.ndarray] = []
 
     def _alloc(self, n: int) -> np.ndarray:
@@ -140,8 +145,10 @@ class Builder:
         slots = self._alloc(n)
         tokens = self.rng.integers(*CACHED_TOKEN_RANGE, size=n).astype(np.int32)
         shape = (n, self.hkv, self.d)
-        self.k_pool[slots] = normal_bf16(self.rng, shape)
-        self.v_pool[slots] = normal_bf16(self.rng, shape)
+        k, v = normal_bf16(self.rng, shape), normal_bf16(self.rng, shape)
+        if self.values:
+            self.k_pool[slots] = k
+            self.v_pool[slots] = v
         return Run(slots, tokens, True)
 
     def new(self, n: int) -> Run:
@@ -216,7 +223,8 @@ def _slots(runs: Sequence[Run]) -> np.ndarray:
 def extend_workload(seed: int, num_q_heads: int, num_kv_heads: int, *, n_groups: int,
                     members: int, prefix: int, ext_lo: int, ext_hi: int,
                     own_cached_hi: int = 0, ungrouped: int = 0, ungrouped_prefix: int = 0,
-                    pool_size: Optional[int] = None, name: str = "extend") -> Workload:
+                    pool_size: Optional[int] = None, name: str = "extend",
+                    values: bool = True) -> Workload:
     """Groups of `members` requests share a cached `prefix`; each request may also hold
     U[0, own_cached_hi] cached tokens of its own, then extends U[ext_lo, ext_hi] new tokens.
     `ungrouped` more requests have their own cached prefix of `ungrouped_prefix` tokens."""
@@ -226,7 +234,7 @@ def extend_workload(seed: int, num_q_heads: int, num_kv_heads: int, *, n_groups:
     own = rng.integers(0, own_cached_hi + 1, size=n_req) if own_cached_hi > 0 else np.zeros(n_req, np.int64)
     need = n_groups * prefix + int(ext.sum()) + int(own.sum()) + ungrouped * ungrouped_prefix
     P = pool_size if pool_size is not None else max(4096, 1 << int(np.ceil(np.log2(need * 1.25 + 1))))
-    b = Builder(rng, num_q_heads, num_kv_heads, P)
+    b = Builder(rng, num_q_heads, num_kv_heads, P, values=values)
     rows, pl, grp, toks, new_runs, cached_seqs = [], [], [], [], [], []
     gpl = []
     i = 0
@@ -268,7 +276,8 @@ def extend_workload(seed: int, num_q_heads: int, num_kv_heads: int, *, n_groups:
 
 def decode_workload(seed: int, num_q_heads: int, num_kv_heads: int, *, n_groups: int,
                     members: int, prefix: int, dist_lo: int, dist_hi: int,
-                    ungrouped: int = 0, min_pool: int = 0, name: str = "decode") -> Workload:
+                    ungrouped: int = 0, min_pool: int = 0, name: str = "decode",
+                    values: bool = True) -> Workload:
     """Groups of `members` requests share a cached `prefix`; each request holds U[dist_lo,
     dist_hi] distinct tokens of which the last is the current token (stored in the step).
     `ungrouped` more requests hold only distinct tokens."""
@@ -277,7 +286,7 @@ def decode_workload(seed: int, num_q_heads: int, num_kv_heads: int, *, n_groups:
     dist = rng.integers(dist_lo, dist_hi + 1, size=n_req)
     need = n_groups * prefix + int(dist.sum())
     P = max(min_pool, need) if min_pool else max(4096, 1 << int(np.ceil(np.log2(need * 1.25 + 1))))
-    b = Builder(rng, num_q_heads, num_kv_heads, P)
+    b = Builder(rng, num_q_heads, num_kv_heads, P, values=values)
     rows, sl, grp, gpl, new_runs, cached_seqs = [], [], [], [], [], []
     i = 0
     for g in range(n_groups):
@@ -353,7 +362,7 @@ def paged_workload(seed: int, num_q_heads: int, num_kv_heads: int, *, page: int,
 def tree_workload(seed: int, num_q_heads: int, num_kv_heads: int, *, depth: int, fanout: int,
                   seg_lo: int, seg_hi: int, p_empty: float, n_decode: int, tail_hi: int,
                   n_extend: int, own_hi: int, ext_lo: int, ext_hi: int,
-                  name: str = "tree") -> Workload:
+                  name: str = "tree", values: bool = True) -> Workload:
     """A random radix tree of cached segments (a node's segment U[seg_lo, seg_hi] tokens, empty
     with probability p_empty; 1..fanout children per node down to `depth` levels) declared as a
     group forest.  Decode requests sit on random nodes with U[0, tail_hi] cached tokens of their
@@ -378,7 +387,7 @@ def tree_workload(seed: int, num_q_heads: int, num_kv_heads: int, *, depth: int,
     ext_new = rng.integers(ext_lo, ext_hi + 1, size=n_extend)
     need = sum(seg_len) + int(dec_tail.sum()) + n_decode + int(ext_own.sum()) + int(ext_new.sum())
     P = max(4096, 1 << int(np.ceil(np.log2(need * 1.25 + 1))))
-    b = Builder(rng, num_q_heads, num_kv_heads, P)
+    b = Builder(rng, num_q_heads, num_kv_heads, P, values=values)
     runs = [b.cached(n) if n > 0 else None for n in seg_len]
     plen = []
     for nd in range(n_nodes):
@@ -429,7 +438,7 @@ def tree_workload(seed: int, num_q_heads: int, num_kv_heads: int, *, depth: int,
 
 def chunked_prefill_workload(seed: int, num_q_heads: int, num_kv_heads: int, *, system: int,
                              prompt: int, chunk: int, n_decode: int, tail_lo: int, tail_hi: int,
-                             name: str = "chunked-prefill") -> Workload:
+                             name: str = "chunked-prefill", values: bool = True) -> Workload:
     """Mixed token batching with chunked prefill: after a cached system prompt of `system` tokens,
     one request's `prompt`-token prompt is prefilled `chunk` tokens per step; in every step
     `n_decode` running requests (the same system prompt, then an own cached tail of U[tail_lo,
@@ -439,7 +448,7 @@ def chunked_prefill_workload(seed: int, num_q_heads: int, num_kv_heads: int, *, 
     n_steps = (prompt + chunk - 1) // chunk
     pool = system + prompt + n_decode * (tail_hi + n_steps) + 64
     pool = max(4096, (pool + 1023) // 1024 * 1024)
-    b = Builder(rng, num_q_heads, num_kv_heads, pool)
+    b = Builder(rng, num_q_heads, num_kv_heads, pool, values=values)
     sp = b.cached(system)
     chunks = [b.new(min(chunk, prompt - i * chunk)) for i in range(n_steps)]
     tails = [b.cached(int(rng.integers(tail_lo, tail_hi + 1))) for _ in range(n_decode)]
@@ -466,19 +475,20 @@ def chunked_prefill_workload(seed: int, num_q_heads: int, num_kv_heads: int, *, 
                     f"random permutation")
 
 
-def llama3_chunked_prefill(seed: int = 1006) -> Workload:
+def llama3_chunked_prefill(seed: int = 1006, values: bool = True) -> Workload:
     """32 q / 8 kv heads; a 6144-token prompt prefilled 2048 tokens per step beside 64 decode
     requests on a shared 1024-token system prompt (own tails U[200,1000])."""
     return chunked_prefill_workload(seed, 32, 8, system=1024, prompt=6144, chunk=2048,
                                     n_decode=64, tail_lo=200, tail_hi=1000,
-                                    name="llama3-chunked-prefill-6144x2048-64dec")
+                                    name="llama3-chunked-prefill-6144x2048-64dec",
+                                    values=values)
 
 
-def tiny(seed: int = 1001) -> Workload:
+def tiny(seed: int = 1001, values: bool = True) -> Workload:
     """8 q / 2 kv heads; one cached 1000-token prefix in a 4096-slot pool; 4 requests extend 40
     new tokens each (causal), then 8 decode steps of one token per request."""
     rng = np.random.default_rng(seed)
-    b = Builder(rng, 8, 2, 4096)
+    b = Builder(rng, 8, 2, 4096, values=values)
     pre = b.cached(1000)
     ext = [b.new(40) for _ in range(4)]
     dec = [[b.new(1) for _ in range(8)] for _ in range(4)]
@@ -493,26 +503,28 @@ def tiny(seed: int = 1001) -> Workload:
                     f"8 decode steps; pool 4096 slots, random permutation")
 
 
-def llama7b_extend(seed: int = 1002) -> Workload:
+def llama7b_extend(seed: int = 1002, values: bool = True) -> Workload:
     """32/32 heads; 4 groups x 16 requests on a cached 2000-token prefix; each extends U[40,200]."""
     return extend_workload(seed, 32, 32, n_groups=4, members=16, prefix=2000, ext_lo=40,
-                           ext_hi=200, pool_size=32768, name="llama7b-extend-4x16-p2000")
+                           ext_hi=200, pool_size=32768, name="llama7b-extend-4x16-p2000",
+                           values=values)
 
 
-def llama7b_decode_hf(seed: int = 1003) -> Workload:
+def llama7b_decode_hf(seed: int = 1003, values: bool = True) -> Workload:
     """32/32 heads; 16 groups x 16 requests on a 2000-token prefix; distinct U[100,500]."""
     return decode_workload(seed, 32, 32, n_groups=16, members=16, prefix=2000, dist_lo=100,
-                           dist_hi=500, name="llama7b-decode-16x16-p2000")
+                           dist_hi=500, name="llama7b-decode-16x16-p2000", values=values)
 
 
-def llama3_gqa_decode(seed: int = 1004) -> Workload:
+def llama3_gqa_decode(seed: int = 1004, values: bool = True) -> Workload:
     """32 q / 8 kv heads; 16 groups x 16 requests on a 16000-token prefix; distinct U[200,1000];
     pool of at least 409,600 slots."""
     return decode_workload(seed, 32, 8, n_groups=16, members=16, prefix=16000, dist_lo=200,
-                           dist_hi=1000, min_pool=409600, name="llama3-gqa-decode-16x16-p16000")
+                           dist_hi=1000, min_pool=409600, name="llama3-gqa-decode-16x16-p16000",
+                           values=values)
 
 
-def radix_mixed(seed: int = 1005, tree: bool = True) -> Workload:
+def radix_mixed(seed: int = 1005, tree: bool = True, values: bool = True) -> Workload:
     """Radix tree 1000 -> 8 x 500 -> 4 x 200 per branch (32 leaves).  One step: 16 leaf requests
     extend 64 tokens; 8 cache misses run a 1500-token full prefill; 40 decode requests, request j on
     leaf j mod 32 with its own tail of U[1,32] tokens (the last one current).
@@ -521,7 +533,7 @@ def radix_mixed(seed: int = 1005, tree: bool = True) -> Workload:
     system prompt, one level."""
     rng = np.random.default_rng(seed)
     tails = rng.integers(1, 33, size=40)
-    b = Builder(rng, 32, 32, 32768)
+    b = Builder(rng, 32, 32, 32768, values=values)
     sysp = b.cached(1000)
     branch = [b.cached(500) for _ in range(8)]
     leaf = [b.cached(200) for _ in range(32)]

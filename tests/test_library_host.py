@@ -197,7 +197,7 @@ def test_plan_launch_counts(librx):
     assert p.launches() == 2
     rx.decode_plan(p, d, list(range(8)), [300] * 8, [0] * 8, [200])  # 32 rows and own keys
     assert p.launches() == 3
-    wl = W.NAMED["radix-mixed"]()
+    wl = W.radix_mixed(values=False)  # tables and lengths only
     dc = wl.steps[0].decode
     dd = _desc(rows=wl.req_to_token.shape[0], stride=wl.req_to_token.shape[1],
                hq=wl.num_q_heads, hkv=wl.num_kv_heads, pool=wl.pool_size)
@@ -267,7 +267,7 @@ def test_tree_decode_plan_reads_each_node_once(librx):
 
 def test_radix_mixed_tree_plans(librx):
     from prefix_shared_kv_gb300 import workloads as W
-    wl, wl1 = W.NAMED["radix-mixed"](), W.NAMED["radix-mixed-1level"]()
+    wl, wl1 = W.radix_mixed(values=False), W.radix_mixed(tree=False, values=False)
     reads = []
     for w in (wl, wl1):
         dc, e = w.steps[0].decode, w.steps[0].extend

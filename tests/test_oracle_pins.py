@@ -365,7 +365,7 @@ def test_batchllm_token_saving_printed_values():
 
 def test_optimal_hit_rate_of_the_radix_mixed_tree_by_simulation():
     """1 - C / sum(prefill) equals the hit rate of running the tree's leaves in DFS order."""
-    wl = W.radix_mixed()
+    wl = W.radix_mixed(values=False)  # token sequences only
     leaves = wl.cached_sequences[:32]
     s = radix.PrefixStore()
     cached = total = 0

@@ -100,7 +100,7 @@ def test_workload_tables_and_slots_pass(librx, kind):
                              n_decode=20, tail_hi=30, n_extend=5, own_hi=20, ext_lo=1,
                              ext_hi=40)
     else:
-        wl = W.NAMED["radix-mixed"]()
+        wl = W.radix_mixed(values=False)
     for st in wl.steps:
         rx.check_slots(st.store_slots, wl.pool_size)
         if st.extend is not None:

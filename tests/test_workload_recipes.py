@@ -1,7 +1,9 @@
 """The benchmark's named workloads have the shapes their recipes state (head counts, request
 counts, prefix / extend / distinct lengths, shared-prefix structure, pool slots), and the work the
 benchmark divides by (extend FLOPs over unmasked pairs, unique decode KV bytes, store bytes) is
-what those shapes give.  Host only."""
+what those shapes give.  Host only.  The full-size workloads are built structure-only
+(values=False: the same draws in the same order, cached KV not written into pools), which the
+first test shows gives the same tables, slots, lengths and inputs as the full build."""
 import os
 import sys
 
@@ -39,6 +41,24 @@ def distinct_tokens_have_distinct_slots(wl):
     return True
 
 
+def test_structure_only_builds_are_the_benchmarks_workloads():
+    assert W.NAMED["extend"] is W.llama7b_extend and W.NAMED["decode"] is W.llama7b_decode_hf
+    assert W.NAMED["gqa-decode"] is W.llama3_gqa_decode and W.NAMED["radix-mixed"] is W.radix_mixed
+    assert W.NAMED["chunked-prefill"] is W.llama3_chunked_prefill
+    for make in (W.tiny, lambda values: W.tree_workload(
+            3, 8, 8, depth=3, fanout=2, seg_lo=0, seg_hi=60, p_empty=0.2, n_decode=12,
+            tail_hi=9, n_extend=5, own_hi=7, ext_lo=1, ext_hi=20, values=values)):
+        a, b = make(values=True), make(values=False)
+        assert b.k_pool.shape[0] == 0 and np.array_equal(a.req_to_token, b.req_to_token)
+        for sa, sb in zip(a.steps, b.steps):
+            assert np.array_equal(sa.store_slots, sb.store_slots)
+            assert np.array_equal(sa.k_new, sb.k_new) and np.array_equal(sa.v_new, sb.v_new)
+            for xa, xb in ((sa.extend, sb.extend), (sa.decode, sb.decode)):
+                assert (xa is None) == (xb is None)
+                if xa is not None:
+                    assert np.array_equal(xa.q, xb.q) and np.array_equal(xa.req_idx, xb.req_idx)
+
+
 def test_tiny():
     wl = W.tiny()
     assert (wl.num_q_heads, wl.num_kv_heads, wl.pool_size) == (8, 2, 4096)
@@ -52,7 +72,7 @@ def test_tiny():
 
 
 def test_extend_workload():
-    wl = W.NAMED["extend"]()
+    wl = W.llama7b_extend(values=False)
     e = wl.steps[0].extend
     assert (wl.num_q_heads, wl.num_kv_heads) == (32, 32) and len(e.req_idx) == 64
     assert (e.prefix_len == 2000).all() and e.extend_len.min() >= 40 and e.extend_len.max() <= 200
@@ -69,7 +89,7 @@ def test_extend_workload():
     ("decode", 32, 2000, 100, 500, 108800),
     ("gqa-decode", 8, 16000, 200, 1000, 409600)])
 def test_decode_workloads(name, hkv, prefix, lo, hi, tokens):
-    wl = W.NAMED[name]()
+    wl = W.NAMED[name](values=False)
     d = wl.steps[0].decode
     assert (wl.num_q_heads, wl.num_kv_heads) == (32, hkv) and len(d.req_idx) == 256
     own = d.seq_len - prefix
@@ -87,7 +107,7 @@ def test_decode_workloads(name, hkv, prefix, lo, hi, tokens):
 
 
 def test_radix_mixed():
-    wl = W.NAMED["radix-mixed"]()
+    wl = W.radix_mixed(values=False)
     st = wl.steps[0]
     e, d = st.extend, st.decode
     assert (wl.num_q_heads, wl.num_kv_heads, wl.pool_size) == (32, 32, 32768)
@@ -116,7 +136,7 @@ def test_radix_mixed():
 
 
 def test_chunked_prefill():
-    wl = W.NAMED["chunked-prefill"]()
+    wl = W.llama3_chunked_prefill(values=False)
     assert (wl.num_q_heads, wl.num_kv_heads) == (32, 8) and len(wl.steps) == 3
     for i, st in enumerate(wl.steps):
         e, d = st.extend, st.decode
