@@ -10,7 +10,10 @@ requests), the one batch that exercises every part of the path.
 Printed metric (one JSON line on rank 0): `value` = extend FLOPs of the batch divided by the device
 time of the whole step (store + extend + decode), in TFLOP/s; `parts` gives each part against its
 own roofline (decode: unique KV bytes / time vs HBM; extend: FLOPs / time vs bf16 tensor peak;
-store: bytes moved / time).  Decode-only workloads report decode GB/s instead.
+store: bytes moved / time).  Decode-only workloads report decode GB/s instead.  `per_workload`
+adds the extend, decode and gqa-decode configurations, each timed the same way in the same
+process (their pools filled with N(0,1) bf16 on the device, so that the host does not draw
+gigabytes of KV), with its own parts and clock record.
 
 Timing: W warm-up steps, then K steps, each bracketed by CUDA events on the launch stream with an
 L2 flush between steps (outside the events: a 256 MiB buffer written, then another read, so no
@@ -217,6 +220,9 @@ def parse_args():
     ap.add_argument("--workload", default="radix-mixed", choices=sorted(W.NAMED))
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-workload", action="store_true",
+                    help="skip timing the extend / decode / gqa-decode configurations beside "
+                         "the main workload")
     ap.add_argument("--only", choices=["store", "extend", "decode"], default=None,
                     help="time one part alone (profiling runs)")
     return ap.parse_args()
@@ -322,7 +328,6 @@ def main():
     w = work_counts(wl)
     peaks, peak_src = load_peaks()
     dw = DeviceWorkload(wl, dev)
-    stream = torch.cuda.current_stream(dev)
     # L2 flush between steps, outside the timed region: write a 256 MiB buffer (twice the L2), then
     # read another one, so that the written lines are back in DRAM before the next step starts
     # (left dirty in L2, their write-back would be timed inside the step's first kernel)
@@ -333,23 +338,120 @@ def main():
         flush_w.zero_()
         flush_r.max()
 
+    only = [args.only] if args.only else None
+    m = measure(dw, w, args, dev, pg, flush_l2, peaks, only)
+    ms_max, part_ms, pdesc, clk, t_wall = m["ms_max"], m["part_ms"], m["parts"], m["clocks"], m["wall"]
+    has_ext, has_dec = m["has_ext"], m["has_dec"]
+    units_per_step = w["extend_flops"] if has_ext else (w["decode_kv_bytes"] if has_dec else w["store_bytes"])
+    scale = 1e12 if has_ext else 1e9
+    unit = "TFLOP/s" if has_ext else "GB/s"
+    value = world * units_per_step / (ms_max * 1e-3) / scale
+    value_is = ("the batch's extend FLOPs (unmasked causal pairs x 4 d Hq) / device time of the "
+                "whole step (store + extend + decode); each part against its own roofline is in "
+                "'parts'" if has_ext else
+                "unique decode KV bytes / device time of the whole step (store + decode); each "
+                "part against its own roofline is in 'parts'")
+
+    if has_ext:
+        dom = ("extend", "extend_attn.cu")
+        roof = {"bound": "tensor", "achieved": pdesc["extend"]["TFLOP/s"],
+                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": pdesc["extend"]["frac_bf16"]}
+    elif has_dec:
+        dom = ("decode", "decode_attn.cu")
+        roof = {"bound": "hbm", "achieved": pdesc["decode"]["GB/s"], "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": pdesc["decode"]["frac_hbm"]}
+    else:
+        dom = ("store", "store_kv.cu")
+        roof = {"bound": "hbm", "achieved": pdesc["store"]["GB/s"], "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": pdesc["store"]["frac_hbm"]}
+    roof["kernel"] = dom[0]
+    roof["peak_source"] = f"{peak_src} (burst)" if roof["unit"] == "TFLOP/s" else peak_src
+    roof["traffic"] = recorded_traffic(dom[1], wl.name)
+    roof["traffic_source"] = (
+        "recorded: dram__bytes_read.sum + dram__bytes_write.sum per launch from an earlier ncu "
+        "capture of this kernel source (hash) on this workload, profiles/dram_traffic.txt; not "
+        "measured in this run" if roof["traffic"] is not None else
+        "none: no ncu capture recorded for this kernel source and workload")
+
+    gpu_launches = args.steps * m["launches_per_step"]
+
+    # ---- the other configurations, timed the same way in this process ---------------------
+    per_workload = None
+    if not args.only and not args.no_per_workload:
+        per_workload = {}
+        del dw
+        torch.cuda.empty_cache()
+        for name in ("extend", "decode", "gqa-decode"):
+            if name == args.workload:
+                continue
+            # structure-only build (slots, lengths, new tokens' KV, queries drawn on the host as
+            # for the parity tests); every pool slot filled with N(0,1) bf16 on the device
+            pwl = W.NAMED[name](values=False)
+            pw = work_counts(pwl)
+            pdw = DeviceWorkload(pwl, dev, pool_seed=7000 + len(name))
+            pm = measure(pdw, pw, args, dev, pg, flush_l2, peaks, None)
+            per_workload[name] = {"workload": pwl.name, "recipe": pwl.recipe,
+                                  "ms_per_step": pm["ms_max"], "parts": pm["parts"],
+                                  "clocks": pm["clocks"],
+                                  "pools": "every slot N(0,1) bf16, filled on the device"}
+            gpu_launches += args.steps * pm["launches_per_step"]
+            del pdw
+            torch.cuda.empty_cache()
+        dw = DeviceWorkload(wl, dev)
+
+    # ---- end to end through the public API with host buffers -----------------------------
+    e2e = None
+    if not args.no_e2e and not args.only:
+        e2e = run_e2e(wl, dw, dev, args, pg, world, w, unit, scale, has_ext)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.only:  # N = 1 only
+        er, dr, est, sample, threads = oracle_sample_rate(wl, budget_s=12.0)
+        cpu = {"value": er if has_ext else dr, "unit": unit, "cores": threads, "kind": "oracle",
+               "sample": sample}
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": unit, "value_is": value_is,
+                "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "bf16", "data": "synthetic",
+                "config": {"workload": wl.name, "recipe": wl.recipe,
+                           "parallelism": f"replicas x{world}",
+                           "l2": "between timed steps a 256 MiB buffer written, then another "
+                                 "256 MiB buffer read (outside the timed region)"},
+                "parts": pdesc, "roofline": roof, "gpu_launches": gpu_launches,
+                "clocks": clk, "e2e": e2e, "cpu_baseline": cpu, "wall_timed_s": t_wall,
+                "per_workload": per_workload}
+        if args.only:
+            line["only"] = args.only
+        print(json.dumps(line), flush=True)
+    if pg is not None:
+        pg.destroy_process_group()
+    return 0
+
+
+def measure(dw, w, args, dev, pg, flush_l2, peaks, only):
+    """W warm-up steps, then K timed steps of the workload's parts (CUDA events on the launch
+    stream around every part, the L2 flush between steps outside the events, nvidia-smi clock
+    samples during the timed steps); the step time is the maximum over ranks."""
+    import torch
+    wl = dw.wl
+    stream = torch.cuda.current_stream(dev)
     parts = [("store", dw.store), ("extend", dw.extend), ("decode", dw.decode)]
-    if args.only:
-        parts = [p for p in parts if p[0] == args.only]
-
-    def step():
-        for _, f in parts:
-            f(0)
-
+    if only:
+        parts = [p for p in parts if p[0] in only]
     for _ in range(max(args.warmup, 0)):
         flush_l2()
-        step()
+        for _, f in parts:
+            f(0)
     torch.cuda.synchronize(dev)
     barrier(pg, dev)
     torch.cuda.synchronize(dev)
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(parts) + 1)]
           for _ in range(args.steps)]
-    clocks = ClockSampler(local)
+    clocks = ClockSampler(dev.index if dev.index is not None else 0)
     clocks.start()
     t_wall = time.perf_counter()
     for k in range(args.steps):
@@ -366,16 +468,9 @@ def main():
     step_ms = [ev[k][0].elapsed_time(ev[k][-1]) for k in range(args.steps)]
     part_ms = {name: statistics.mean(ev[k][j].elapsed_time(ev[k][j + 1]) for k in range(args.steps))
                for j, (name, _) in enumerate(parts)}
-    ms = statistics.mean(step_ms)
-    ms_max = allreduce_max(pg, ms, dev)
-
+    ms_max = allreduce_max(pg, statistics.mean(step_ms), dev)
     has_ext = w["extend_flops"] > 0 and "extend" in part_ms
     has_dec = w["decode_kv_bytes"] > 0 and "decode" in part_ms
-    units_per_step = w["extend_flops"] if has_ext else (w["decode_kv_bytes"] if has_dec else w["store_bytes"])
-    scale = 1e12 if has_ext else 1e9
-    unit = "TFLOP/s" if has_ext else "GB/s"
-    value = world * units_per_step / (ms_max * 1e-3) / scale
-
     pdesc = {}
     if "store" in part_ms:
         a = w["store_bytes"] / (part_ms["store"] * 1e-3) / 1e9
@@ -398,60 +493,14 @@ def main():
                            # a group counts twice): the kernel's own bandwidth is plan bytes / ms
                            "plan_kv_bytes": float(dw.steps[0].dec_plan.key_reads())
                            * wl.head_dim * 2 * 2}
-    if has_ext:
-        dom = ("extend", "extend_attn.cu")
-        roof = {"bound": "tensor", "achieved": pdesc["extend"]["TFLOP/s"],
-                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                "frac": pdesc["extend"]["frac_bf16"]}
-    elif has_dec:
-        dom = ("decode", "decode_attn.cu")
-        roof = {"bound": "hbm", "achieved": pdesc["decode"]["GB/s"], "peak": peaks["hbm_gbs"],
-                "unit": "GB/s", "frac": pdesc["decode"]["frac_hbm"]}
-    else:
-        dom = ("store", "store_kv.cu")
-        roof = {"bound": "hbm", "achieved": pdesc["store"]["GB/s"], "peak": peaks["hbm_gbs"],
-                "unit": "GB/s", "frac": pdesc["store"]["frac_hbm"]}
-    roof["kernel"] = dom[0]
-    roof["peak_source"] = f"{peak_src} (burst)" if roof["unit"] == "TFLOP/s" else peak_src
-    roof["traffic"] = recorded_traffic(dom[1], wl.name)
-
-    # kernels of ours per step, as the plans report them (a decode plan launches its tensor-core
-    # units, its mma.sync units and the merge)
+    # kernels of ours per step, as the plans report them
     st0 = dw.steps[0]
-    launches_per_step = {
-        "store": int(wl.steps[0].store_slots.shape[0] > 0),
-        "extend": st0.ext_plan.launches() if st0.ext_plan is not None else 0,
-        "decode": st0.dec_plan.launches() if st0.dec_plan is not None else 0}
-    gpu_launches = args.steps * sum(launches_per_step[n] for n, _ in parts)
-
-    # ---- end to end through the public API with host buffers -----------------------------
-    e2e = None
-    if not args.no_e2e and not args.only:
-        e2e = run_e2e(wl, dw, dev, args, pg, world, w, unit, scale, has_ext)
-
-    cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.only:  # N = 1 only
-        er, dr, est, sample, threads = oracle_sample_rate(wl, budget_s=12.0)
-        cpu = {"value": er if has_ext else dr, "unit": unit, "cores": threads, "kind": "oracle",
-               "sample": sample}
-
-    if rank == 0:
-        line = {"metric": METRIC, "value": value, "unit": unit, "n_gpus": world,
-                "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
-                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-                "dtype": "bf16", "data": "synthetic",
-                "config": {"workload": wl.name, "recipe": wl.recipe,
-                           "parallelism": f"replicas x{world}",
-                           "l2": "between timed steps a 256 MiB buffer written, then another "
-                                 "256 MiB buffer read (outside the timed region)"},
-                "parts": pdesc, "roofline": roof, "gpu_launches": gpu_launches,
-                "clocks": clk, "e2e": e2e, "cpu_baseline": cpu, "wall_timed_s": t_wall}
-        if args.only:
-            line["only"] = args.only
-        print(json.dumps(line), flush=True)
-    if pg is not None:
-        pg.destroy_process_group()
-    return 0
+    per = {"store": int(wl.steps[0].store_slots.shape[0] > 0),
+           "extend": st0.ext_plan.launches() if st0.ext_plan is not None else 0,
+           "decode": st0.dec_plan.launches() if st0.dec_plan is not None else 0}
+    return {"ms_max": ms_max, "part_ms": part_ms, "parts": pdesc, "clocks": clk, "wall": t_wall,
+            "has_ext": has_ext, "has_dec": has_dec,
+            "launches_per_step": sum(per[n] for n, _ in parts)}
 
 
 def run_e2e(wl, dw, dev, args, pg, world, w, unit, scale, has_ext):

@@ -49,18 +49,45 @@ class DevStep:
     dec_lse: Optional[torch.Tensor] = None
 
 
+def fill_normal_bf16(t: torch.Tensor, seed: int) -> None:
+    """Fill a bf16 device tensor with fp32 N(0,1) draws rounded to bf16 (round-to-nearest-even)
+    from a seeded torch generator on the tensor's device, a chunk at a time."""
+    g = torch.Generator(device=t.device)
+    g.manual_seed(seed)
+    flat = t.view(-1)
+    step = 1 << 26
+    for s in range(0, flat.numel(), step):
+        n = min(step, flat.numel() - s)
+        flat[s:s + n] = torch.randn(n, generator=g, device=t.device,
+                                    dtype=torch.float32).to(torch.bfloat16)
+
+
 def workspace(nbytes: int, device) -> torch.Tensor:
     # torch's caching allocator returns 512-byte aligned blocks
     return torch.empty(max(256, nbytes), dtype=torch.uint8, device=device)
 
 
 class DeviceWorkload:
-    def __init__(self, wl: Workload, device="cuda", stream=None):
+    """`pool_seed`: for a workload built structure-only (values=False, no cached KV drawn on the
+    host), the pools are allocated on the device and every slot is filled with N(0,1) bf16 values
+    from this seed (K with pool_seed, V with pool_seed + 1).  Used where only timing matters;
+    parity checks use host-drawn pools, which the oracle reads too."""
+
+    def __init__(self, wl: Workload, device="cuda", stream=None, pool_seed=None):
         self.wl = wl
         self.device = torch.device(device)
         self.stream = stream
-        self.k_pool = to_bf16(wl.k_pool, self.device)
-        self.v_pool = to_bf16(wl.v_pool, self.device)
+        if wl.k_pool.shape[0] == 0 and wl.pool_size > 0:
+            if pool_seed is None:
+                raise ValueError("structure-only workload: pass pool_seed to fill its pools")
+            shape = (wl.pool_size, wl.num_kv_heads, wl.head_dim)
+            self.k_pool = torch.empty(shape, dtype=torch.bfloat16, device=self.device)
+            self.v_pool = torch.empty(shape, dtype=torch.bfloat16, device=self.device)
+            fill_normal_bf16(self.k_pool, pool_seed)
+            fill_normal_bf16(self.v_pool, pool_seed + 1)
+        else:
+            self.k_pool = to_bf16(wl.k_pool, self.device)
+            self.v_pool = to_bf16(wl.v_pool, self.device)
         self.r2t = to_i32(wl.req_to_token, self.device)
         self.desc = rx.kv_desc(wl.num_q_heads, wl.num_kv_heads, wl.pool_size, self.r2t,
                                wl.softmax_scale)

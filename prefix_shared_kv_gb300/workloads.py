@@ -117,11 +117,17 @@ class Builder:
 
     def __init__(self, rng: np.random.Generator, num_q_heads: int, num_kv_heads: int,
                  pool_size: int, head_dim: int = HEAD_DIM, page: int = 1, values: bool = True):
-        # values=False: the same draws in the same order (so the same slots, lengths, tokens and
-        # new tokens' KV), but the cached KV is not written into pools (structure-only checks of
-        # full-size workloads, without allocating their pools)
+        # values=False: the same slots, lengths, tokens, new tokens' KV and queries, but no cached
+        # KV is drawn or written into pools (structure-only checks of full-size workloads without
+        # allocating their pools; device runs whose pools are filled on the GPU)
         self.values = values
         self.rng = rng
+        # the values come from streams of their own, seeded from the structure stream: one for the
+        # cached KV (not drawn at all by structure-only builds), one for the new tokens' KV and the
+        # queries; so values=False changes no other draw and builds in a fraction of the time
+        s_cached, s_new = rng.integers(0, 2 ** 63, size=2)
+        self.crng = np.random.default_rng(int(s_cached))
+        self.nrng = np.random.default_rng(int(s_new))
         self.hq, self.hkv, self.d = num_q_heads, num_kv_heads, head_dim
         self.pool_size = pool_size
         self.page = page
@@ -144,18 +150,18 @@ class Builder:
     def cached(self, n: int) -> Run:
         slots = self._alloc(n)
         tokens = self.rng.integers(*CACHED_TOKEN_RANGE, size=n).astype(np.int32)
-        shape = (n, self.hkv, self.d)
-        k, v = normal_bf16(self.rng, shape), normal_bf16(self.rng, shape)
         if self.values:
-            self.k_pool[slots] = k
-            self.v_pool[slots] = v
+            shape = (n, self.hkv, self.d)
+            self.k_pool[slots] = normal_bf16(self.crng, shape)
+            self.v_pool[slots] = normal_bf16(self.crng, shape)
         return Run(slots, tokens, True)
 
     def new(self, n: int) -> Run:
         slots = self._alloc(n)
         tokens = self.rng.integers(*NEW_TOKEN_RANGE, size=n).astype(np.int32)
         shape = (n, self.hkv, self.d)
-        return Run(slots, tokens, False, normal_bf16(self.rng, shape), normal_bf16(self.rng, shape))
+        return Run(slots, tokens, False, normal_bf16(self.nrng, shape),
+                   normal_bf16(self.nrng, shape))
 
     def row(self, runs: Sequence[Run]) -> int:
         self.rows.append(np.concatenate([r.slots for r in runs]).astype(np.int32)
@@ -163,7 +169,7 @@ class Builder:
         return len(self.rows) - 1
 
     def q(self, n_rows: int) -> np.ndarray:
-        return normal_bf16(self.rng, (n_rows, self.hq, self.d))
+        return normal_bf16(self.nrng, (n_rows, self.hq, self.d))
 
     def finish(self, name: str, steps_spec, cached_sequences, recipe: str) -> Workload:
         """steps_spec: list of (new_runs, extend_spec, decode_spec) with row ids; rows are then
@@ -588,6 +594,6 @@ NAMED = {
     "decode": llama7b_decode_hf,
     "gqa-decode": llama3_gqa_decode,
     "radix-mixed": radix_mixed,
-    "radix-mixed-1level": lambda: radix_mixed(tree=False),
+    "radix-mixed-1level": lambda values=True: radix_mixed(tree=False, values=values),
     "chunked-prefill": llama3_chunked_prefill,
 }
