@@ -2,8 +2,8 @@
 
 Tolerances (bf16 in, fp32 accumulate, bf16 out): O max-abs <= 2e-2 and mean-abs <= 2e-3, LSE
 within 1e-3; the pool scatter is bit-exact.  Small cases are compared element by element over every
-row; the full-size workloads, run in the benchmark's launch configuration, are compared on a
-sample of requests that the oracle computes one by one.
+row; the full-size workloads, run in the benchmark's launch configuration, are compared on every
+row, except the two decode workloads, compared on a stratified set of requests.
 """
 import numpy as np
 import pytest
@@ -42,7 +42,27 @@ def oracle_pools(wl, upto_step):
     return kp, vp
 
 
-def run_and_check(wl, cuda, sample=None, seed=0):
+def stratified_decode_requests(d):
+    """Decode requests that cover a batch's structure: in every group the members with the
+    shortest and the longest own part, one request at every decile of the own lengths over the
+    batch, and every request outside a group (a cache miss)."""
+    grp = np.asarray(d.group_of_req)
+    gpl = np.asarray(d.group_prefix_len)
+    own = np.asarray(d.seq_len) - np.where(grp >= 0, gpl[np.maximum(grp, 0)], 0)
+    pick = set(np.flatnonzero(grp < 0).tolist())
+    for g in np.unique(grp[grp >= 0]):
+        m = np.flatnonzero(grp == g)
+        pick.add(int(m[np.argmin(own[m])]))
+        pick.add(int(m[np.argmax(own[m])]))
+    order = np.argsort(own, kind="stable")
+    for q in range(11):
+        pick.add(int(order[min(len(order) - 1, q * (len(order) - 1) // 10)]))
+    return sorted(pick)
+
+
+def run_and_check(wl, cuda, sample=None, seed=0, decode_pick=None):
+    """Run every step of `wl` on the GPU and compare with the oracle: every row, or the rows of
+    `sample` random requests per batch, or (decode only) the requests decode_pick(batch) names."""
     dw = DeviceWorkload(wl, cuda)
     rng = np.random.default_rng(seed)
     for i, st in enumerate(wl.steps):
@@ -64,7 +84,9 @@ def run_and_check(wl, cuda, sample=None, seed=0):
         if st.decode is not None:
             d = st.decode
             reqs = None
-            if sample is not None and len(d.req_idx) > sample:
+            if decode_pick is not None:
+                reqs = decode_pick(d)
+            elif sample is not None and len(d.req_idx) > sample:
                 reqs = sorted(rng.choice(len(d.req_idx), sample, replace=False))
             o, l = A.decode(d.q, kp, vp, wl.req_to_token, d.req_idx, d.seq_len, wl.softmax_scale,
                             requests=reqs)
@@ -450,14 +472,24 @@ def test_block_granular_pool(cuda, hq, hkv, prefix):
 
 
 # ---------------------------------------------------------------------------------------------
-# Full-size workloads in the benchmark's configuration, sampled requests.
+# Full-size workloads in the benchmark's configuration.  Every extend and decode row of the
+# extend, radix-mixed (tree and one-level) and chunked-prefill workloads; for the two decode
+# workloads, whose oracle reads up to 17,000 keys per request, a stratified set of requests
+# (every group's shortest and longest member, every own-length decile, every ungrouped request).
 # ---------------------------------------------------------------------------------------------
 
-@pytest.mark.parametrize("name", ["extend", "decode", "gqa-decode", "radix-mixed",
-                                  "radix-mixed-1level", "chunked-prefill"])
-def test_full_size_workloads_sampled(cuda, name):
+@pytest.mark.parametrize("name", ["extend", "radix-mixed", "radix-mixed-1level",
+                                  "chunked-prefill"])
+def test_full_size_workloads_every_row(cuda, name):
+    run_and_check(W.NAMED[name](), cuda)
+
+
+@pytest.mark.parametrize("name", ["decode", "gqa-decode"])
+def test_full_size_decode_workloads_stratified(cuda, name):
     wl = W.NAMED[name]()
-    run_and_check(wl, cuda, sample=6, seed=1)
+    picked = stratified_decode_requests(wl.steps[0].decode)
+    assert len(picked) >= 2 * 16  # both ends of every group at least
+    run_and_check(wl, cuda, decode_pick=stratified_decode_requests)
 
 
 # ---------------------------------------------------------------------------------------------
@@ -479,6 +511,42 @@ def test_bounded_wait_times_out_and_the_context_stays_usable(cuda):
     torch.cuda.synchronize()
     assert status.item() == rx.RX_ERR_TIMEOUT
     run_and_check(W.tiny(), cuda)                        # kernels still run and agree
+
+
+@pytest.mark.parametrize("hq,hkv", [(32, 32), (32, 8)])
+def test_table_entry_outside_the_pool_is_flagged(cuda, hq, hkv):
+    """An entry of req_to_token outside the pool is not read (the kernels read zeros instead) and
+    sets RX_ERR_RANGE in the workspace status word; rx_read_status reports and clears it.  Checked
+    for the extend kernel and, in a shared prefix (tensor-core units at gq = 4, mma.sync units at
+    gq = 1) and in a request's own keys, for the decode kernels."""
+    ext = W.extend_workload(60 + hkv, hq, hkv, n_groups=2, members=4, prefix=600, ext_lo=10,
+                            ext_hi=90, ungrouped=1, ungrouped_prefix=300)
+    dec = W.decode_workload(70 + hkv, hq, hkv, n_groups=2, members=9, prefix=900, dist_lo=20,
+                            dist_hi=300, ungrouped=2)
+    for wl, kind in ((ext, "extend"), (dec, "decode")):
+        dw = DeviceWorkload(wl, cuda)
+        dw.store(0)
+        ds = dw.steps[0]
+        b = wl.steps[0].extend if kind == "extend" else wl.steps[0].decode
+        run = dw.extend if kind == "extend" else dw.decode
+        ws = ds.ext_ws if kind == "extend" else ds.dec_ws
+        grp = np.asarray(b.group_of_req)
+        for where in ("shared prefix", "own keys"):
+            saved = dw.r2t.clone()
+            if where == "shared prefix":
+                for r in np.flatnonzero(grp == 0):  # every member's row, so they stay equal
+                    dw.r2t[int(b.req_idx[r]), 123] = wl.pool_size + 3
+            else:
+                r = int(np.flatnonzero(grp < 0)[0])
+                n = int(b.prefix_len[r] + b.extend_len[r]) if kind == "extend" else int(b.seq_len[r])
+                dw.r2t[int(b.req_idx[r]), n // 2] = wl.pool_size + 3
+            run(0)
+            assert rx.read_status(ws) == rx.RX_ERR_RANGE, (kind, where)
+            assert rx.read_status(ws) == rx.RX_OK
+            dw.r2t.copy_(saved)
+            run(0)
+            assert rx.read_status(ws) == rx.RX_OK
+    run_and_check(W.tiny(), cuda)  # the context still runs and agrees
 
 
 # ---------------------------------------------------------------------------------------------
