@@ -214,14 +214,24 @@ rx_status rx_decode_attn(const rx_plan* plan, const rx_kv_desc* desc, const void
  *             rx_plan_workspace_size) is rejected with RX_ERR_WORKSPACE before anything runs.
  *   others    as for rx_decode_attn (caller-owned device tensors; work enqueued on `stream`).
  * The first call on a device sets up the scratch's device address for that device; make it before
- * any stream capture.  All calls share the one array: calls whose work overlaps on the GPU (other
- * streams, other host threads) race on it and must not be issued.  Device-side errors are recorded
- * in the scratch and cleared by the next call; they cannot be read back with rx_read_status.
+ * any stream capture.  The tables are copied in from the plan's pinned staging buffer, as
+ * rx_plan_upload does; like that call, it first waits (on the host) for the plan's previous copy
+ * to finish.  All calls share the one array: calls whose work overlaps on the GPU (other streams,
+ * other host threads) race on it and must not be issued.
+ * Device-side errors (a table entry outside the pool: RX_ERR_RANGE; a bounded wait that ran out:
+ * RX_ERR_TIMEOUT) are recorded in the scratch's status word, which the next call resets; read
+ * them after the call and before the next one with rx_noalloc_read_status.
  * ------------------------------------------------------------------------------------------- */
 #define RX_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
 rx_status rx_decode_attn_noalloc(const rx_plan* plan, const rx_kv_desc* desc, const void* k_pool,
                                  const void* v_pool, const void* q, void* o, float* lse,
                                  rx_stream_t stream);
+/* rx_noalloc_read_status: as rx_read_status, for the scratch of rx_decode_attn_noalloc on the
+ * current device: waits for `stream`, copies the status word of the last call enqueued before it
+ * into *status (host; RX_OK or the first device-side error) and clears it.  Allocates nothing. */
+rx_status rx_noalloc_read_status(int32_t* status, rx_stream_t stream);
+/* rx_noalloc_scratch_bytes: RX_NOALLOC_SCRATCH_BYTES as compiled into the library. */
+size_t rx_noalloc_scratch_bytes(void);
 
 /* ---------------------------------------------------------------------------------------------
  * Validation (host; a checking mode for callers and debug builds).  The attention and store

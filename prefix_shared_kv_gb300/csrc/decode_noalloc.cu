@@ -11,10 +11,12 @@
 // address with cudaGetSymbolAddress (a host-side name of the array is not a device address) and
 // caches it for later calls on that device.  Make that first call before any stream capture.
 //
-// Sharing: every call uses the same array.  Each call first copies the plan's tables into it,
-// which also resets the device status word to zero; the partial results need no clearing (each is
-// written before it is read).  Two calls whose work overlaps on the GPU (different streams, or
-// different host threads) race on the array and must not be issued.
+// Sharing: every call uses the same array.  Each call first copies the plan's tables into it
+// (through the plan's pinned staging buffer, as rx_plan_upload does for a workspace), which also
+// resets the device status word to zero; the partial results need no clearing (each is written
+// before it is read).  Two calls whose work overlaps on the GPU (different streams, or different
+// host threads) race on the array and must not be issued.  A call's device-side errors stay in
+// the array's status word until the next call: rx_noalloc_read_status reads them.
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -59,16 +61,24 @@ extern "C" rx_status rx_decode_attn_noalloc(const rx_plan* plan, const rx_kv_des
   void* scratch = nullptr;
   rx_status st = scratch_of_current_device(&scratch);
   if (st) return st;
-  const void* blob = nullptr;
-  size_t blob_bytes = 0;
   rx::PlanHeader h;
-  st = rx::plan_for_noalloc(plan, desc, k_pool, v_pool, q, o, lse, scratch, kScratchBytes, &blob,
-                            &blob_bytes, &h);
+  st = rx::plan_for_noalloc(plan, desc, k_pool, v_pool, q, o, lse, scratch, kScratchBytes, &h);
   if (st) return st;
-  cudaError_t e = cudaMemcpyAsync(scratch, blob, blob_bytes, cudaMemcpyHostToDevice,
-                                  (cudaStream_t)stream);
-  if (e != cudaSuccess) return rx::set_error(RX_ERR_CUDA, cudaGetErrorString(e));
+  // the tables go in from pinned memory, so the copy does not hold the host until the stream
+  // drains (a copy straight from the plan's pageable buffer would)
+  st = rx_plan_upload(plan, scratch, kScratchBytes, stream);
+  if (st) return st;
   const int le = rx::launch_decode(desc, &h, k_pool, v_pool, q, o, lse, scratch, stream);
   if (le) return rx::set_error(RX_ERR_CUDA, cudaGetErrorString((cudaError_t)le));
   return RX_OK;
 }
+
+extern "C" rx_status rx_noalloc_read_status(int32_t* status, rx_stream_t stream) {
+  if (!status) return rx::set_error(RX_ERR_INVALID, "status is NULL");
+  void* scratch = nullptr;
+  rx_status st = scratch_of_current_device(&scratch);
+  if (st) return st;
+  return rx_read_status(scratch, status, stream);
+}
+
+extern "C" size_t rx_noalloc_scratch_bytes(void) { return kScratchBytes; }

@@ -169,8 +169,7 @@ rx_status rx::set_error(rx_status st, const char* msg) { return fail(st, "%s", m
 
 rx_status rx::plan_for_noalloc(const rx_plan* plan, const rx_kv_desc* desc, const void* k,
                                const void* v, const void* q, const void* o, const void* lse,
-                               const void* scratch, size_t scratch_bytes, const void** blob,
-                               size_t* blob_bytes, PlanHeader* hdr) {
+                               const void* scratch, size_t scratch_bytes, PlanHeader* hdr) {
   if (plan && plan->kind == 2 && plan->ws_bytes > scratch_bytes)
     return fail(RX_ERR_WORKSPACE,
                 "rx_decode_attn_noalloc: the plan needs %zu bytes of scratch, the library holds "
@@ -178,8 +177,6 @@ rx_status rx::plan_for_noalloc(const rx_plan* plan, const rx_kv_desc* desc, cons
                 plan->ws_bytes, scratch_bytes);
   rx_status st = check_plan_use(plan, 2, desc, k, v, q, o, lse, scratch, scratch_bytes);
   if (st) return st;
-  *blob = plan->blob.data();
-  *blob_bytes = plan->blob.size();
   *hdr = plan->hdr();
   return RX_OK;
 }

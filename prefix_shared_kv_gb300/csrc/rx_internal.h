@@ -125,10 +125,9 @@ int launch_attn_items(const rx_kv_desc* d, const ExtItem* items, const ExtRow* r
 rx_status set_error(rx_status st, const char* msg);
 // Checks a decode plan and the call's tensors for rx_decode_attn_noalloc, with the library's own
 // scratch (`scratch`, `scratch_bytes`) in place of a caller workspace; on success returns the
-// tables to copy into the scratch and the plan header.
+// plan header.
 rx_status plan_for_noalloc(const rx_plan* plan, const rx_kv_desc* desc, const void* k,
                            const void* v, const void* q, const void* o, const void* lse,
-                           const void* scratch, size_t scratch_bytes, const void** blob,
-                           size_t* blob_bytes, PlanHeader* hdr);
+                           const void* scratch, size_t scratch_bytes, PlanHeader* hdr);
 
 }  // namespace rx

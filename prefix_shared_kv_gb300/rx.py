@@ -25,7 +25,8 @@ EXPORTED = [
     "rx_plan_rows",
     "rx_extend_plan",
     "rx_extend_plan_tree", "rx_extend_attn", "rx_decode_plan", "rx_decode_plan_tree",
-    "rx_decode_attn", "rx_decode_attn_noalloc", "rx_read_status", "rx_selftest_wait_timeout",
+    "rx_decode_attn", "rx_decode_attn_noalloc", "rx_noalloc_read_status",
+    "rx_noalloc_scratch_bytes", "rx_read_status", "rx_selftest_wait_timeout",
     "rx_check_slots", "rx_check_tables", "rx_radix_create", "rx_radix_destroy",
     "rx_radix_insert", "rx_radix_match", "rx_radix_stats", "rx_radix_acquire", "rx_radix_release",
     "rx_radix_evict", "rx_slot_pool_create", "rx_slot_pool_destroy", "rx_slot_pool_free_count",
@@ -86,6 +87,8 @@ def lib():
         "rx_decode_attn": (C.c_int, [_P, C.POINTER(KVDesc), _P, _P, _P, _P, _P, _P, C.c_size_t,
                                      _P]),
         "rx_decode_attn_noalloc": (C.c_int, [_P, C.POINTER(KVDesc), _P, _P, _P, _P, _P, _P]),
+        "rx_noalloc_read_status": (C.c_int, [_I32P, _P]),
+        "rx_noalloc_scratch_bytes": (C.c_size_t, []),
         "rx_read_status": (C.c_int, [_P, _I32P, _P]),
         "rx_selftest_wait_timeout": (C.c_int, [_P, C.c_int64, _P]),
         "rx_radix_create": (C.c_int, [C.POINTER(_P)]),
@@ -314,7 +317,17 @@ def decode_attn_noalloc(plan: Plan, desc: KVDesc, k_pool, v_pool, q, o, lse, str
                                         _ptr(q), _ptr(o), _ptr(lse), _stream(stream)))
 
 
-NOALLOC_SCRATCH_BYTES = 64 << 20
+def noalloc_scratch_bytes() -> int:
+    """rx_noalloc_scratch_bytes: the largest plan rx_decode_attn_noalloc takes."""
+    return int(lib().rx_noalloc_scratch_bytes())
+
+
+def noalloc_read_status(stream=None) -> int:
+    """rx_noalloc_read_status: the status word of the last rx_decode_attn_noalloc call on the
+    current device (waits for `stream`; clears the word)."""
+    s = C.c_int32(0)
+    _check(lib().rx_noalloc_read_status(C.byref(s), _stream(stream)))
+    return s.value
 
 
 def read_status(workspace, stream=None) -> int:

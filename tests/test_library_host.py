@@ -29,6 +29,13 @@ def test_library_exports_every_declared_symbol(librx):
     assert sorted(rx.EXPORTED) == names
 
 
+def test_noalloc_scratch_size_is_the_headers(librx):
+    text = open(os.path.join(ROOT, "include", "rx.h")).read()
+    m = re.search(r"#define RX_NOALLOC_SCRATCH_BYTES \(\(size_t\)(\d+) << (\d+)\)", text)
+    assert m, "RX_NOALLOC_SCRATCH_BYTES not found in rx.h"
+    assert rx.noalloc_scratch_bytes() == int(m.group(1)) << int(m.group(2))
+
+
 def test_radix_matches_oracle_on_random_sequences(librx):
     rng = np.random.default_rng(0)
     for trial in range(60):
