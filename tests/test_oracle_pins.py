@@ -21,6 +21,22 @@ def _bf(bits):
     return float(A.bf16_to_f64(np.asarray([bits], np.uint16))[0])
 
 
+def test_bf16_decoding_matches_torch_on_every_bit_pattern():
+    """The oracle's bf16 -> float64 decoding (which the brute-force pins below use too) against
+    torch's own bfloat16 -> float64 conversion, on all 65,536 bit patterns: zeros of both signs,
+    subnormals, infinities and NaNs included."""
+    torch = pytest.importorskip("torch")
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    ours = A.bf16_to_f64(bits)
+    ref = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).double().numpy()
+    nan = np.isnan(ref)
+    assert (np.isnan(ours) == nan).all() and nan.sum() == 2 * 127  # exponent 255, mantissa != 0
+    assert np.array_equal(ours[~nan], ref[~nan])
+    assert np.array_equal(np.signbit(ours[~nan]), np.signbit(ref[~nan]))  # -0.0 stays -0.0
+    assert ours[0x3F80] == 1.0 and ours[0xC000] == -2.0 and ours[0x0001] == 2.0 ** -133
+    assert ours[0x7F80] == np.inf and ours[0xFF80] == -np.inf
+
+
 def brute_row(qrow_bits, keys_bits, vals_bits, scale):
     """Attention of one query over a list of key/value rows, written as plain loops."""
     d = len(qrow_bits)
