@@ -190,6 +190,11 @@ rx_status rx_plan_key_reads(const rx_plan* plan, int64_t* rows);
  * scored against all members' queries; each member's remaining keys are read by other thread
  * blocks of the same launch, and the partial softmax states are combined by a log-sum-exp merge.
  * seq_len[b] >= 1 and >= group_prefix_len[group_of_req[b]].  Arrays of rx_decode_plan are (host).
+ * rx_decode_attn: when a plan has work for both partial kernels (tensor-core shared-prefix units
+ * and mma.sync units), the call runs the mma.sync units on a second stream that the plan owns,
+ * forked from and joined back to `stream` with events, so that neither kernel's last wave idles
+ * the GPU.  Calls that share one plan share that stream: give callers on different streams (or
+ * host threads) plans of their own, and they never wait on one another.
  * ------------------------------------------------------------------------------------------- */
 rx_status rx_decode_plan(rx_plan* plan, const rx_kv_desc* desc, int32_t batch,
                          const int32_t* req_idx, const int32_t* seq_len,

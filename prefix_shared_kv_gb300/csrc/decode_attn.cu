@@ -18,7 +18,6 @@
 #include <math_constants.h>
 
 #include <atomic>
-#include <mutex>
 
 #include "ptx.cuh"
 #include "rx_internal.h"
@@ -43,7 +42,9 @@ struct DecParams {
 };
 
 constexpr int kThreads = 256;
-constexpr int kStageHalf = 128 * kHeadDim * 2;  // one of K / V per stage: 32 KiB
+constexpr int kStageHalf = kDecRows * kHeadDim * 2;  // one of K / V per stage: 32 KiB
+static_assert(kDecRows == 128 && 2 * kStageHalf == kDecStageBytes,
+              "the tilings below stage 128 (head, key) rows of K and of V");
 
 template <int MT, int HB>
 __device__ __forceinline__ void load_stage(const DecParams& p, const DecItem& it,
@@ -316,29 +317,17 @@ __global__ void __launch_bounds__(32 * kMergeWarps) decode_merge_kernel(
         tot > 0.f ? (mx + __log2f(tot)) * 0.69314718055994530942f : -CUDART_INF_F;
 }
 
-// A second stream per device on which the tensor-core shared-prefix units run beside the mma.sync
-// units (fork and join through events, so the pair also works under stream capture): each kernel's
-// last wave would otherwise leave SMs idle.  Created on first use; the lock serialises the
-// record / wait sequence of concurrent callers.
-struct AuxStream {
-  cudaStream_t stream = nullptr;
-  cudaEvent_t fork = nullptr, join = nullptr;
-};
-constexpr int kMaxDevices = 64;
-AuxStream g_aux[kMaxDevices];
-std::mutex g_aux_lock;
-
 }  // namespace
 
 int launch_decode(const rx_kv_desc* d, const PlanHeader* h, const void* k_pool,
                   const void* v_pool, const void* q, void* o, float* lse, void* ws,
-                  void* stream) {
+                  void* stream, const AuxStream* aux) {
   // kernel attributes belong to the current device: set once per device (bit d of the mask)
   static std::atomic<uint64_t> attr_set{0};
   int cur = 0;
   cudaError_t de = cudaGetDevice(&cur);
   if (de != cudaSuccess) return (int)de;
-  if (cur < 0 || cur >= kMaxDevices) return (int)cudaErrorInvalidDevice;
+  if (cur < 0 || cur >= 64) return (int)cudaErrorInvalidDevice;
   if (!((attr_set.load() >> cur) & 1)) {
     cudaError_t e = cudaFuncSetAttribute(decode_partial_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -372,31 +361,22 @@ int launch_decode(const rx_kv_desc* d, const PlanHeader* h, const void* k_pool,
         nullptr, nullptr, p.part_o, p.part_lse, p.status, st);
   };
   if (h->n_xitems > 0 && h->n_items > 0) {
-    int dev = 0;
-    cudaError_t ce = cudaGetDevice(&dev);
-    if (ce != cudaSuccess) return (int)ce;
-    if (dev < 0 || dev >= kMaxDevices) return (int)cudaErrorInvalidDevice;
-    std::lock_guard<std::mutex> lock(g_aux_lock);
-    AuxStream& a = g_aux[dev];
-    if (!a.stream) {
-      ce = cudaStreamCreateWithFlags(&a.stream, cudaStreamNonBlocking);
-      if (ce == cudaSuccess) ce = cudaEventCreateWithFlags(&a.fork, cudaEventDisableTiming);
-      if (ce == cudaSuccess) ce = cudaEventCreateWithFlags(&a.join, cudaEventDisableTiming);
-      if (ce != cudaSuccess) return (int)ce;
-    }
     // The tensor-core kernel takes whole SMs (one CTA fills an SM's shared memory), so it goes
     // first, on the caller's stream with nothing to wait for; the mma.sync units follow on the
-    // second stream and fill the other SMs.
-    ce = cudaEventRecord(a.fork, s);
+    // plan's second stream (fork and join through events, so the pair also works under stream
+    // capture) and fill the other SMs.  Each kernel's last wave would otherwise leave SMs idle.
+    if (!aux || !aux->stream || !aux->fork || !aux->join) return (int)cudaErrorInvalidValue;
+    cudaStream_t a = (cudaStream_t)aux->stream;
+    cudaError_t ce = cudaEventRecord((cudaEvent_t)aux->fork, s);
     if (ce != cudaSuccess) return (int)ce;
     const int e = run_x(s);
     if (e) return e;
-    ce = cudaStreamWaitEvent(a.stream, a.fork, 0);
+    ce = cudaStreamWaitEvent(a, (cudaEvent_t)aux->fork, 0);
     if (ce != cudaSuccess) return (int)ce;
-    decode_partial_kernel<<<h->n_items, kThreads, kDecSmemBytes, a.stream>>>(p);
+    decode_partial_kernel<<<h->n_items, kThreads, kDecSmemBytes, a>>>(p);
     ce = cudaGetLastError();
-    if (ce == cudaSuccess) ce = cudaEventRecord(a.join, a.stream);
-    if (ce == cudaSuccess) ce = cudaStreamWaitEvent(s, a.join, 0);
+    if (ce == cudaSuccess) ce = cudaEventRecord((cudaEvent_t)aux->join, a);
+    if (ce == cudaSuccess) ce = cudaStreamWaitEvent(s, (cudaEvent_t)aux->join, 0);
     if (ce != cudaSuccess) return (int)ce;
   } else if (h->n_xitems > 0) {
     const int e = run_x(s);

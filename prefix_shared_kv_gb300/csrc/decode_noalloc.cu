@@ -68,7 +68,10 @@ extern "C" rx_status rx_decode_attn_noalloc(const rx_plan* plan, const rx_kv_des
   // drains (a copy straight from the plan's pageable buffer would)
   st = rx_plan_upload(plan, scratch, kScratchBytes, stream);
   if (st) return st;
-  const int le = rx::launch_decode(desc, &h, k_pool, v_pool, q, o, lse, scratch, stream);
+  rx::AuxStream aux;
+  st = rx::plan_aux_stream(plan, &aux);
+  if (st) return st;
+  const int le = rx::launch_decode(desc, &h, k_pool, v_pool, q, o, lse, scratch, stream, &aux);
   if (le) return rx::set_error(RX_ERR_CUDA, cudaGetErrorString((cudaError_t)le));
   return RX_OK;
 }

@@ -102,12 +102,27 @@ struct rx_plan {
   mutable cudaEvent_t staged = nullptr;
   mutable int staged_dev = -1;
   mutable bool staged_pending = false;
+  // decode: the second stream on which a call runs its mma.sync units beside the tensor-core
+  // units, with its fork / join events; created on first use, on that call's device, and owned by
+  // the plan (so callers with plans of their own never serialise on a shared stream)
+  mutable cudaStream_t aux = nullptr;
+  mutable cudaEvent_t aux_fork = nullptr, aux_join = nullptr;
+  mutable int aux_dev = -1;
+  void drop_aux() const {
+    if (aux_fork) cudaEventDestroy(aux_fork);
+    if (aux_join) cudaEventDestroy(aux_join);
+    if (aux) cudaStreamDestroy(aux);
+    aux = nullptr;
+    aux_fork = aux_join = nullptr;
+    aux_dev = -1;
+  }
   ~rx_plan() {
     if (staged) {
       if (staged_pending) cudaEventSynchronize(staged);
       cudaEventDestroy(staged);
     }
     if (pinned) cudaFreeHost(pinned);
+    drop_aux();
   }
   PlanHeader hdr() const {
     PlanHeader h;
@@ -166,6 +181,30 @@ rx_status check_plan_use(const rx_plan* p, int kind, const rx_kv_desc* d, const 
 }  // namespace
 
 rx_status rx::set_error(rx_status st, const char* msg) { return fail(st, "%s", msg); }
+
+rx_status rx::plan_aux_stream(const rx_plan* plan, AuxStream* out) {
+  out->stream = out->fork = out->join = nullptr;
+  const PlanHeader h = plan->hdr();
+  if (!(h.n_xitems > 0 && h.n_items > 0)) return RX_OK;  // one kernel: no second stream
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e) return cuda_fail(e, "decode: current device");
+  if (plan->aux && plan->aux_dev != dev) plan->drop_aux();  // streams belong to one device
+  if (!plan->aux) {
+    e = cudaStreamCreateWithFlags(&plan->aux, cudaStreamNonBlocking);
+    if (!e) e = cudaEventCreateWithFlags(&plan->aux_fork, cudaEventDisableTiming);
+    if (!e) e = cudaEventCreateWithFlags(&plan->aux_join, cudaEventDisableTiming);
+    if (e) {
+      plan->drop_aux();
+      return cuda_fail(e, "decode: second stream");
+    }
+    plan->aux_dev = dev;
+  }
+  out->stream = plan->aux;
+  out->fork = plan->aux_fork;
+  out->join = plan->aux_join;
+  return RX_OK;
+}
 
 rx_status rx::plan_for_noalloc(const rx_plan* plan, const rx_kv_desc* desc, const void* k,
                                const void* v, const void* q, const void* o, const void* lse,
@@ -396,7 +435,7 @@ rx_status rx_decode_plan_tree(rx_plan* plan, const rx_kv_desc* desc, int32_t bat
 
   auto chunks = [&](int len, int kind, std::vector<std::pair<int, int>>& out) {
     const int hb = std::min(hb_of(kind), hkv);
-    const int nk = 128 / hb_of(kind);
+    const int nk = kDecRows / hb_of(kind);
     int max_keys = (int)(target / (hb * key_bytes));
     max_keys = std::max(64, std::min(kDecMaxKeysPerItem, max_keys));
     const int n = (len + max_keys - 1) / max_keys;
@@ -571,7 +610,10 @@ rx_status rx_decode_attn(const rx_plan* plan, const rx_kv_desc* desc, const void
                                 workspace_bytes);
   if (st) return st;
   const PlanHeader h = plan->hdr();
-  const int e = launch_decode(desc, &h, k_pool, v_pool, q, o, lse, workspace, stream);
+  AuxStream aux;
+  st = plan_aux_stream(plan, &aux);
+  if (st) return st;
+  const int e = launch_decode(desc, &h, k_pool, v_pool, q, o, lse, workspace, stream, &aux);
   return e ? cuda_fail(e, "decode launch") : RX_OK;
 }
 

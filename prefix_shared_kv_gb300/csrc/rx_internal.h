@@ -42,7 +42,8 @@ struct DecMergeRef {    // one partial of a request
 
 constexpr int kDecMaxKeysPerItem = 2048;
 constexpr int kDecStages = 3;
-constexpr int kDecStageBytes = 2 * 128 * kHeadDim * 2;   // K + V, 128 rows each
+constexpr int kDecRows = 128;                              // (head, key) rows per stage
+constexpr int kDecStageBytes = 2 * kDecRows * kHeadDim * 2;   // K + V, 128 rows each
 constexpr size_t kDecSmemBytes = (size_t)kDecStages * kDecStageBytes + kDecMaxKeysPerItem * 4;
 
 // ---------------------------------------------------------------------------------------------
@@ -104,12 +105,21 @@ struct PlanHeader {
 };
 static_assert(sizeof(PlanHeader) == 256, "header is 256 bytes");
 
+// A second stream (and its fork / join events) on which a decode call runs its mma.sync units
+// beside the tensor-core units; owned by the plan, created on the device of its first use.
+// All NULL when the plan's calls need no second stream.
+struct AuxStream {
+  void* stream;
+  void* fork;
+  void* join;
+};
+
 // Launchers (defined in the .cu files).  Return cudaError_t as int.
 int launch_store_kv(const rx_kv_desc* d, void* k_pool, void* v_pool, const void* k_new,
                     const void* v_new, const int32_t* slots, int64_t n, void* stream);
 int launch_decode(const rx_kv_desc* d, const PlanHeader* h, const void* k_pool,
                   const void* v_pool, const void* q, void* o, float* lse, void* ws,
-                  void* stream);
+                  void* stream, const AuxStream* aux);
 int launch_extend(const rx_kv_desc* d, const PlanHeader* h, const void* k_pool,
                   const void* v_pool, const void* q, void* o, float* lse, void* ws,
                   void* stream);
@@ -121,6 +131,9 @@ int launch_attn_items(const rx_kv_desc* d, const ExtItem* items, const ExtRow* r
                       const void* q, void* o, float* lse, float* part_o, float* part_lse,
                       int32_t* status, void* stream);
 
+// The plan's second stream for a decode call on the current device (created on first use); all
+// NULL when the plan's calls launch a single kernel.
+rx_status plan_aux_stream(const rx_plan* plan, AuxStream* out);
 // Records `msg` as the calling thread's last error and returns `st`.
 rx_status set_error(rx_status st, const char* msg);
 // Checks a decode plan and the call's tensors for rx_decode_attn_noalloc, with the library's own

@@ -226,6 +226,35 @@ def test_unit_values_give_unit_output(cuda, kind):
             _within_one_ulp_of_one(dw.steps[i].dec_o, f"{kind} decode")
 
 
+def test_decode_calls_with_their_own_plans_on_two_streams(cuda):
+    """Two callers, each with a plan of its own whose decode runs both partial kernels (a second
+    stream per plan), issue their calls on two streams without waiting for each other, several
+    times over; every result matches the oracle."""
+    def make(seed):
+        return W.tree_workload(seed, 8, 8, depth=2, fanout=3, seg_lo=50, seg_hi=300, p_empty=0.0,
+                               n_decode=40, tail_hi=40, n_extend=1, own_hi=30, ext_lo=1,
+                               ext_hi=10)
+    wls = [make(41), make(43)]
+    streams = [torch.cuda.Stream(cuda), torch.cuda.Stream(cuda)]
+    dws = [DeviceWorkload(wl, cuda, stream=st) for wl, st in zip(wls, streams)]
+    for dw in dws:
+        assert dw.steps[0].dec_plan.launches() == 3
+        with torch.cuda.stream(dw.stream):
+            dw.store(0)
+    torch.cuda.synchronize()
+    for _ in range(4):
+        for dw in dws:
+            with torch.cuda.stream(dw.stream):
+                dw.decode(0)
+    torch.cuda.synchronize()
+    for wl, dw in zip(wls, dws):
+        st = wl.steps[0]
+        kp, vp = A.store_kv(wl.k_pool, wl.v_pool, st.k_new, st.v_new, st.store_slots)
+        d = st.decode
+        o, l = A.decode(d.q, kp, vp, wl.req_to_token, d.req_idx, d.seq_len, wl.softmax_scale)
+        assert_close(dw.steps[0].dec_o, dw.steps[0].dec_lse, o, l, what=wl.name)
+
+
 def test_cuda_graph_replay_of_a_step(cuda):
     """A whole step -- store, extend, and a decode whose tensor-core and mma.sync units run on
     two streams (fork and join through events) before the merge -- captured once into a CUDA
