@@ -276,6 +276,16 @@ rx_status rx_read_status(const void* workspace, int32_t* status, rx_stream_t str
  * RX_ERR_TIMEOUT in *status (device, int32, first error wins: clear it to 0 first).  The GPU and
  * the context stay usable.  For tests of the timeout path. */
 rx_status rx_selftest_wait_timeout(int32_t* status, int64_t limit_ns, rx_stream_t stream);
+/* rx_selftest_pair_mma: the tensor-core steps of the extend kernel that runs on a pair of SMs (a
+ * cluster of two CTAs, tcgen05 .cta_group::2), once, on one cluster, for tests:
+ * s_out = q k^T and o_out = p v, fp32 [256, 128] row-major, from bf16 row-major q [256, 128]
+ * (query rows), k [128, 128] (keys x head dim), v [128, 128], p [256, 128] (query rows x keys);
+ * all device pointers, caller-owned.  info (device, int32[3]): [0] status word, set to RX_OK by
+ * the caller (the kernel records RX_ERR_TIMEOUT there when a bounded wait ran out, and then does
+ * not write the outputs); [1] and [2] the tensor-memory address each CTA of the pair was given.
+ * Enqueued on `stream`. */
+rx_status rx_selftest_pair_mma(const void* q, const void* k, const void* v, const void* p,
+                               float* s_out, float* o_out, int32_t* info, rx_stream_t stream);
 
 /* ---------------------------------------------------------------------------------------------
  * Host radix cache: token sequences -> pool slots, edges labelled with token runs (SGLang

@@ -27,6 +27,7 @@ EXPORTED = [
     "rx_extend_plan_tree", "rx_extend_attn", "rx_decode_plan", "rx_decode_plan_tree",
     "rx_decode_attn", "rx_decode_attn_noalloc", "rx_noalloc_read_status",
     "rx_noalloc_scratch_bytes", "rx_read_status", "rx_selftest_wait_timeout",
+    "rx_selftest_pair_mma",
     "rx_check_slots", "rx_check_tables", "rx_radix_create", "rx_radix_destroy",
     "rx_radix_insert", "rx_radix_match", "rx_radix_stats", "rx_radix_acquire", "rx_radix_release",
     "rx_radix_evict", "rx_slot_pool_create", "rx_slot_pool_destroy", "rx_slot_pool_free_count",
@@ -91,6 +92,7 @@ def lib():
         "rx_noalloc_scratch_bytes": (C.c_size_t, []),
         "rx_read_status": (C.c_int, [_P, _I32P, _P]),
         "rx_selftest_wait_timeout": (C.c_int, [_P, C.c_int64, _P]),
+        "rx_selftest_pair_mma": (C.c_int, [_P, _P, _P, _P, _P, _P, _P, _P]),
         "rx_radix_create": (C.c_int, [C.POINTER(_P)]),
         "rx_radix_destroy": (None, [_P]),
         "rx_radix_insert": (C.c_int, [_P, _I32P, _I32P, C.c_int64, _I64P]),
@@ -452,6 +454,20 @@ def gain_groups(sequences):
                                 grp.ctypes.data_as(_I32P), gpl.ctypes.data_as(_I32P),
                                 ng.ctypes.data_as(_I32P)))
     return grp[:len(seqs)].copy(), gpl[:int(ng[0])].copy()
+
+
+def selftest_pair_mma(q, k, v, p, s_out, o_out, info, stream=None):
+    """rx_selftest_pair_mma: s_out = q k^T, o_out = p v on one SM pair (see rx.h)."""
+    for t, shape in ((q, (256, 128)), (k, (128, 128)), (v, (128, 128)), (p, (256, 128))):
+        if tuple(t.shape) != shape or t.dtype.itemsize != 2 or not t.is_contiguous():
+            raise ValueError(f"bf16 operand of shape {shape} expected")
+    for t in (s_out, o_out):
+        if tuple(t.shape) != (256, 128) or t.dtype.itemsize != 4 or not t.is_contiguous():
+            raise ValueError("fp32 output of shape (256, 128) expected")
+    if info.numel() < 3 or info.dtype.itemsize != 4:
+        raise ValueError("int32 info of 3 elements expected")
+    _check(lib().rx_selftest_pair_mma(_ptr(q), _ptr(k), _ptr(v), _ptr(p), _ptr(s_out),
+                                      _ptr(o_out), _ptr(info), _stream(stream)))
 
 
 def selftest_wait_timeout(status, limit_ns: int, stream=None):
