@@ -225,7 +225,14 @@ def parse_args():
                          "the main workload")
     ap.add_argument("--only", choices=["store", "extend", "decode"], default=None,
                     help="time one part alone (profiling runs)")
+    ap.add_argument("--extend-kernel", choices=["tiles", "pair"], default="tiles",
+                    help="the extend kernel: one SM per item (tiles, the default) or an SM pair")
     return ap.parse_args()
+
+
+def ext_kernel(args):
+    from prefix_shared_kv_gb300 import rx
+    return rx.RX_EXTEND_PAIR if args.extend_kernel == "pair" else rx.RX_EXTEND_TILES
 
 
 def dist_init():
@@ -327,7 +334,7 @@ def main():
     wl = W.NAMED[args.workload]()
     w = work_counts(wl)
     peaks, peak_src = load_peaks()
-    dw = DeviceWorkload(wl, dev)
+    dw = DeviceWorkload(wl, dev, extend_kernel=ext_kernel(args))
     # L2 flush between steps, outside the timed region: write a 256 MiB buffer (twice the L2), then
     # read another one, so that the written lines are back in DRAM before the next step starts
     # (left dirty in L2, their write-back would be timed inside the step's first kernel)
@@ -389,7 +396,8 @@ def main():
             # for the parity tests); every pool slot filled with N(0,1) bf16 on the device
             pwl = W.NAMED[name](values=False)
             pw = work_counts(pwl)
-            pdw = DeviceWorkload(pwl, dev, pool_seed=7000 + len(name))
+            pdw = DeviceWorkload(pwl, dev, pool_seed=7000 + len(name),
+                                 extend_kernel=ext_kernel(args))
             pm = measure(pdw, pw, args, dev, pg, flush_l2, peaks, None)
             per_workload[name] = {"workload": pwl.name, "recipe": pwl.recipe,
                                   "ms_per_step": pm["ms_max"], "parts": pm["parts"],
@@ -398,7 +406,7 @@ def main():
             gpu_launches += args.steps * pm["launches_per_step"]
             del pdw
             torch.cuda.empty_cache()
-        dw = DeviceWorkload(wl, dev)
+        dw = DeviceWorkload(wl, dev, extend_kernel=ext_kernel(args))
 
     # ---- end to end through the public API with host buffers -----------------------------
     e2e = None
@@ -419,6 +427,7 @@ def main():
                 "dtype": "bf16", "data": "synthetic",
                 "config": {"workload": wl.name, "recipe": wl.recipe,
                            "parallelism": f"replicas x{world}",
+                           "extend_kernel": args.extend_kernel,
                            "l2": "between timed steps a 256 MiB buffer written, then another "
                                  "256 MiB buffer read (outside the timed region)"},
                 "parts": pdesc, "roofline": roof, "gpu_launches": gpu_launches,

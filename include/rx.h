@@ -97,6 +97,17 @@ typedef struct rx_plan rx_plan;
 
 rx_status rx_plan_create(rx_plan** out);
 void rx_plan_destroy(rx_plan* plan);
+/* Which tensor-core kernel the extend plans built on `plan` after this call run on (host; the
+ * plan's existing tables are not changed).  Both compute the same attention (within the
+ * extend tolerance); they differ in speed only.
+ *   RX_EXTEND_TILES (default)  one SM per item: two 128-row query tiles, 64-key steps, the two
+ *                              tiles' softmax and MMAs interleaved.
+ *   RX_EXTEND_PAIR             two SMs per item (a cluster of two, tcgen05 cta_group::2): one
+ *                              128-row tile per SM, 128-key steps, M = 256 MMAs.
+ * Any other value returns RX_ERR_INVALID. */
+#define RX_EXTEND_TILES 0
+#define RX_EXTEND_PAIR 1
+rx_status rx_plan_set_extend_kernel(rx_plan* plan, int32_t kernel);
 /* Number of kernels one attention call with the built plan launches (0 for a plan without work;
  * a decode plan launches up to three: tensor-core shared-prefix units, mma.sync units, merge).
  * For a caller's and a benchmark's bookkeeping; (host). */

@@ -771,8 +771,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// Tensor map viewing a pool as [pool_size * num_kv_heads rows, 128 bf16 columns] (row stride
-// 256 bytes), boxes of 64 columns x 1 row, 128-byte swizzle: the unit of tile::gather4.
+}  // namespace
+
 int make_pool_map(CUtensorMap* map, const void* pool, const rx_kv_desc* d) {
   static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
   if (!encode) {
@@ -795,8 +795,6 @@ int make_pool_map(CUtensorMap* map, const void* pool, const rx_kv_desc* d) {
                             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? 0 : (int)cudaErrorInvalidValue;
 }
-
-}  // namespace
 
 int launch_attn_items(const rx_kv_desc* d, const ExtItem* items, const ExtRow* rows,
                       const ExtSeg* segs, int32_t n_items, const void* k_pool, const void* v_pool,
@@ -861,11 +859,15 @@ int launch_extend(const rx_kv_desc* d, const PlanHeader* h, const void* k_pool,
                   const void* v_pool, const void* q, void* o, float* lse, void* ws,
                   void* stream) {
   uint8_t* base = static_cast<uint8_t*>(ws);
-  return launch_attn_items(d, reinterpret_cast<const ExtItem*>(base + h->off_items),
-                           reinterpret_cast<const ExtRow*>(base + h->off_rows),
-                           reinterpret_cast<const ExtSeg*>(base + h->off_segs), h->n_items, k_pool,
-                           v_pool, q, o, lse, nullptr, nullptr,
-                           reinterpret_cast<int32_t*>(base + offsetof(PlanHeader, status)), stream);
+  const ExtItem* items = reinterpret_cast<const ExtItem*>(base + h->off_items);
+  const ExtRow* rows = reinterpret_cast<const ExtRow*>(base + h->off_rows);
+  const ExtSeg* segs = reinterpret_cast<const ExtSeg*>(base + h->off_segs);
+  int32_t* status = reinterpret_cast<int32_t*>(base + offsetof(PlanHeader, status));
+  if (h->ext_kernel == RX_EXTEND_PAIR)
+    return launch_extend_pair(d, items, rows, segs, h->n_items, k_pool, v_pool, q, o, lse, status,
+                              stream);
+  return launch_attn_items(d, items, rows, segs, h->n_items, k_pool, v_pool, q, o, lse, nullptr,
+                           nullptr, status, stream);
 }
 
 }  // namespace rx

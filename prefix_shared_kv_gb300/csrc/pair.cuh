@@ -33,18 +33,20 @@ __device__ __forceinline__ void cluster_sync() {
                    : "memory");
 }
 
-// Arrival on a barrier of another CTA of the cluster (`caddr` from map_to), releasing this
-// thread's earlier writes at cluster scope.
+// Arrival on a barrier of another CTA of the cluster (`caddr` from map_to).  Default semantics
+// (release at CTA scope): what such an arrival publishes is tensor memory or shared memory that
+// the pair's tensor core reads, ordered by the tcgen05 / proxy fences the caller issues before it.
+// Release at cluster scope measured about twice the handoff latency of the whole pipeline.
 __device__ __forceinline__ void arrive_remote(uint32_t caddr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(caddr)
-               : "memory");
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(caddr) : "memory");
 }
 
-// Phase test with acquire at cluster scope (the barrier's arrivals may come from the other CTA).
-__device__ __forceinline__ bool try_wait_cluster(uint32_t mbar, uint32_t parity, uint32_t hint_ns) {
+// Phase test (default semantics: acquire at CTA scope), also for barriers whose arrivals come
+// from the other CTA or from the pair's commits.
+__device__ __forceinline__ bool try_wait_phase(uint32_t mbar, uint32_t parity, uint32_t hint_ns) {
   uint32_t ok;
   asm volatile(
-      "{\n.reg .pred p;\nmbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n"
+      "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
       "selp.u32 %0, 1, 0, p;\n}\n"
       : "=r"(ok)
       : "r"(mbar), "r"(parity), "r"(hint_ns)
@@ -58,14 +60,14 @@ __device__ __forceinline__ uint64_t globaltimer() {
   return t;
 }
 
-// As tc::mbar_wait, with cluster-scope acquire: gives up after `limit_ns` or once *abort is set;
+// As tc::mbar_wait: gives up after `limit_ns` or once *abort is set;
 // on giving up raises *abort, records RX_ERR_TIMEOUT in *status (first error wins), returns false.
 __device__ __forceinline__ bool wait(uint32_t mbar, uint32_t parity, volatile int* abort,
                                      int32_t* status, uint64_t limit_ns) {
-  if (try_wait_cluster(mbar, parity, 0u)) return true;
+  if (try_wait_phase(mbar, parity, 0u)) return true;
   const uint64_t t0 = globaltimer();
   for (;;) {
-    if (try_wait_cluster(mbar, parity, 20000u)) return true;
+    if (try_wait_phase(mbar, parity, 20000u)) return true;
     if (*abort) return false;
     if (globaltimer() - t0 > limit_ns) {
       *abort = 1;
@@ -73,6 +75,19 @@ __device__ __forceinline__ bool wait(uint32_t mbar, uint32_t parity, volatile in
       return false;
     }
   }
+}
+
+// A progress counter in shared memory, published with release and read with acquire (CTA
+// scope).  Plain loads and stores, not barrier operations: a thread that issues MMAs and commits
+// can test it without being held until the tensor pipe has taken the MMAs before its commits,
+// which every mbarrier operation after a commit is.
+__device__ __forceinline__ void st_release(uint32_t saddr, uint32_t v) {
+  asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(saddr), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t ld_acquire(uint32_t saddr) {
+  uint32_t v;
+  asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(saddr) : "memory");
+  return v;
 }
 
 // Tensor memory of the pair: one warp in each of the two CTAs runs these together.

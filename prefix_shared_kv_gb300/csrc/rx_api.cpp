@@ -89,6 +89,7 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 // ---------------------------------------------------------------------------------------------
 struct rx_plan {
   int kind = 0;  // 0 = empty, 1 = extend, 2 = decode
+  int32_t ext_kernel = RX_EXTEND_TILES;  // the kernel extend plans built from now on run on
   std::vector<uint8_t> blob;  // header + tables, uploaded verbatim
   size_t ws_bytes = 0;
   int64_t key_reads = 0;  // (key, KV head) rows of the pool the kernels read
@@ -138,6 +139,10 @@ namespace {
 int32_t attn_steps(int64_t n) { return (int32_t)((n + kAttnKeys - 1) / kAttnKeys); }
 int64_t attn_cost(const ExtItem& it) { return (int64_t)it.n_steps * (it.n_tok[1] > 0 ? 7 : 6); }
 constexpr int64_t kCostClass = 4 * 7;  // four two-tile steps
+// On the SM-pair kernel an item takes steps of kPairKeys keys per segment and costs its steps
+// whether or not it has a second tile (the other CTA gathers and multiplies anyway).
+int32_t pair_steps(int64_t n) { return (int32_t)((n + kPairKeys - 1) / kPairKeys); }
+constexpr int64_t kPairCostClass = 2;  // two steps
 
 template <typename T>
 void put(std::vector<uint8_t>& blob, int64_t off, const std::vector<T>& v) {
@@ -260,6 +265,14 @@ rx_status rx_plan_create(rx_plan** out) {
 }
 
 void rx_plan_destroy(rx_plan* plan) { delete plan; }
+
+rx_status rx_plan_set_extend_kernel(rx_plan* plan, int32_t kernel) {
+  if (!plan) return fail(RX_ERR_INVALID, "plan is NULL");
+  if (kernel != RX_EXTEND_TILES && kernel != RX_EXTEND_PAIR)
+    return fail(RX_ERR_INVALID, "unknown extend kernel");
+  plan->ext_kernel = kernel;
+  return RX_OK;
+}
 
 rx_status rx_plan_key_reads(const rx_plan* plan, int64_t* rows) {
   if (!plan || !rows) return fail(RX_ERR_INVALID, "NULL argument");
@@ -785,6 +798,7 @@ rx_status rx_extend_plan_tree(rx_plan* plan, const rx_kv_desc* desc, int32_t bat
   std::stable_sort(order.begin(), order.end(),
                    [&](size_t a, size_t b) { return units[a].cost > units[b].cost; });
   std::vector<ExtItem> items;
+  const bool pair_kernel = plan->ext_kernel == RX_EXTEND_PAIR;
   int64_t key_reads = 0;
   for (size_t k : order)
     for (const Pair& pr : pairs[k])
@@ -803,15 +817,19 @@ rx_status rx_extend_plan_tree(rx_plan* plan, const rx_kv_desc* desc, int32_t bat
         it.n_seg = pr.n_seg;
         it.kv_head = h;
         it.n_steps = 0;
-        for (int i = 0; i < pr.n_seg; ++i)
-          it.n_steps += attn_steps(segs[pr.seg_begin + i].k_end - segs[pr.seg_begin + i].k_begin);
+        for (int i = 0; i < pr.n_seg; ++i) {
+          const int64_t n = segs[pr.seg_begin + i].k_end - segs[pr.seg_begin + i].k_begin;
+          it.n_steps += pair_kernel ? pair_steps(n) : attn_steps(n);
+        }
         items.push_back(it);
       }
-  // The attention kernel deals the list to its CTAs in rounds (snake order): sorted by falling
-  // cost, every CTA gets a similar total.  The sort is by cost classes four two-tile steps wide,
-  // and keeps the planned order (a unit's KV heads and tiles together) inside a class, so items
-  // that read the same prefix still tend to run at the same time and share it in L2.
-  std::stable_sort(items.begin(), items.end(), [](const ExtItem& a, const ExtItem& b) {
+  // The attention kernel deals the list to its CTAs (clusters) in rounds (snake order): sorted
+  // by falling cost, every CTA gets a similar total.  The sort is by cost classes (four two-tile
+  // steps, or two pair steps) and keeps the planned order (a unit's KV heads and tiles together)
+  // inside a class, so items that read the same prefix still tend to run at the same time and
+  // share it in L2.
+  std::stable_sort(items.begin(), items.end(), [&](const ExtItem& a, const ExtItem& b) {
+    if (pair_kernel) return a.n_steps / kPairCostClass > b.n_steps / kPairCostClass;
     return attn_cost(a) / kCostClass > attn_cost(b) / kCostClass;
   });
   if (items.size() > (size_t)INT32_MAX) return fail(RX_ERR_RANGE, "plan too large");
@@ -820,6 +838,7 @@ rx_status rx_extend_plan_tree(rx_plan* plan, const rx_kv_desc* desc, int32_t bat
   std::memset(&h, 0, sizeof h);
   h.magic = kPlanMagic;
   h.kind = 1;
+  h.ext_kernel = plan->ext_kernel;
   h.n_items = (int32_t)items.size();
   h.num_q_heads = desc->num_q_heads;
   h.num_kv_heads = hkv;

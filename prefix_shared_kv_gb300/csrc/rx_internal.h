@@ -1,7 +1,8 @@
 // Internal tables shared by the host planner (rx_api.cpp) and the kernels (*.cu).
 #pragma once
-#include <stdint.h>
+#include <cuda.h>
 #include <stddef.h>
+#include <stdint.h>
 
 #include "rx.h"
 
@@ -66,8 +67,10 @@ struct ExtSeg {
   int32_t owner;        // -1 = all rows of the item
 };
 
-// Keys per step of the tensor-core attention kernel.
+// Keys per step of the tensor-core attention kernel of decode shared-prefix units (one CTA), and
+// of the extend kernel that runs on a pair of SMs.
 constexpr int kAttnKeys = 64;
+constexpr int kPairKeys = 128;
 
 // Two row tiles (A, B) of the same KV head that walk the same key segments: every K/V step feeds
 // 256 query rows.  Tile B may be empty (n_tok[1] == 0: the CTA runs tile A alone).  The same
@@ -100,7 +103,8 @@ struct PlanHeader {
   // decode plans: shared-prefix units run by the tensor-core attention kernel (ExtItem / ExtRow /
   // ExtSeg tables writing partial rows); n_xitems = 0 when there are none
   int64_t off_xitems, off_xrows, off_xsegs;
-  int32_t n_xitems, pad32;
+  int32_t n_xitems;
+  int32_t ext_kernel;    // extend plans: RX_EXTEND_TILES or RX_EXTEND_PAIR
   int64_t pad[15];
 };
 static_assert(sizeof(PlanHeader) == 256, "header is 256 bytes");
@@ -120,9 +124,18 @@ int launch_store_kv(const rx_kv_desc* d, void* k_pool, void* v_pool, const void*
 int launch_decode(const rx_kv_desc* d, const PlanHeader* h, const void* k_pool,
                   const void* v_pool, const void* q, void* o, float* lse, void* ws,
                   void* stream, const AuxStream* aux);
+// The extend kernel on SM pairs over `n_items` items (one tile per CTA of a pair, kPairKeys-key
+// steps).
 int launch_extend(const rx_kv_desc* d, const PlanHeader* h, const void* k_pool,
                   const void* v_pool, const void* q, void* o, float* lse, void* ws,
                   void* stream);
+int launch_extend_pair(const rx_kv_desc* d, const ExtItem* items, const ExtRow* rows,
+                       const ExtSeg* segs, int32_t n_items, const void* k_pool,
+                       const void* v_pool, const void* q, void* o, float* lse, int32_t* status,
+                       void* stream);
+// Tensor map viewing a pool as [pool_size * num_kv_heads rows, 128 bf16 columns] (row stride
+// 256 bytes), boxes of 64 columns x 1 row, 128-byte swizzle: the unit of tile::gather4.
+int make_pool_map(CUtensorMap* map, const void* pool, const rx_kv_desc* d);
 // The tensor-core attention kernel over `n_items` items of tables in device memory; with
 // part_o != nullptr every tile writes fp32 partial rows (normalised O, base-2 LSE) instead of o /
 // lse.  `status` is the plan's device status word.

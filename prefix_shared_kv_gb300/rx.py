@@ -18,9 +18,11 @@ LIB_PATH = os.path.join(_HERE, "_lib", "librx.so")
 
 RX_OK, RX_ERR_INVALID, RX_ERR_RANGE, RX_ERR_UNSUPPORTED, RX_ERR_CUDA, RX_ERR_TIMEOUT, \
     RX_ERR_WORKSPACE = range(7)
+RX_EXTEND_TILES, RX_EXTEND_PAIR = 0, 1
 
 EXPORTED = [
     "rx_status_string", "rx_last_error", "rx_store_kv", "rx_plan_create", "rx_plan_destroy",
+    "rx_plan_set_extend_kernel",
     "rx_plan_workspace_size", "rx_plan_upload", "rx_plan_key_reads", "rx_plan_launches",
     "rx_plan_rows",
     "rx_extend_plan",
@@ -70,6 +72,7 @@ def lib():
         "rx_store_kv": (C.c_int, [C.POINTER(KVDesc), _P, _P, _P, _P, _P, C.c_int64, _P]),
         "rx_plan_create": (C.c_int, [C.POINTER(_P)]),
         "rx_plan_destroy": (None, [_P]),
+        "rx_plan_set_extend_kernel": (C.c_int, [_P, C.c_int32]),
         "rx_plan_workspace_size": (C.c_int, [_P, C.POINTER(C.c_size_t)]),
         "rx_plan_upload": (C.c_int, [_P, _P, C.c_size_t, _P]),
         "rx_plan_key_reads": (C.c_int, [_P, _I64P]),
@@ -208,6 +211,11 @@ class Plan:
     @property
     def handle(self):
         return self._h
+
+    def set_extend_kernel(self, kernel: int):
+        """rx_plan_set_extend_kernel: RX_EXTEND_TILES (default) or RX_EXTEND_PAIR for the extend
+        plans built from now on."""
+        _check(lib().rx_plan_set_extend_kernel(self._h, int(kernel)))
 
     def workspace_size(self) -> int:
         n = C.c_size_t(0)

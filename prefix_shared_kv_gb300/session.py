@@ -71,9 +71,11 @@ class DeviceWorkload:
     """`pool_seed`: for a workload built structure-only (values=False, no cached KV drawn on the
     host), the pools are allocated on the device and every slot is filled with N(0,1) bf16 values
     from this seed (K with pool_seed, V with pool_seed + 1).  Used where only timing matters;
-    parity checks use host-drawn pools, which the oracle reads too."""
+    parity checks use host-drawn pools, which the oracle reads too.  `extend_kernel`: the
+    tensor-core kernel the extend plans run on (rx.RX_EXTEND_TILES or rx.RX_EXTEND_PAIR)."""
 
-    def __init__(self, wl: Workload, device="cuda", stream=None, pool_seed=None):
+    def __init__(self, wl: Workload, device="cuda", stream=None, pool_seed=None,
+                 extend_kernel=rx.RX_EXTEND_TILES):
         self.wl = wl
         self.device = torch.device(device)
         self.stream = stream
@@ -99,6 +101,7 @@ class DeviceWorkload:
             if st.extend is not None:
                 e = st.extend
                 ds.ext_plan = rx.Plan()
+                ds.ext_plan.set_extend_kernel(extend_kernel)
                 rx.extend_plan(ds.ext_plan, self.desc, e.req_idx, e.prefix_len, e.extend_len,
                                e.group_of_req, e.group_prefix_len, e.group_parent)
                 ds.ext_ws = workspace(ds.ext_plan.workspace_size(), self.device)

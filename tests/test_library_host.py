@@ -396,3 +396,13 @@ def test_plan_rows_and_the_bindings_size_checks(librx):
     rx.decode_plan(p, _desc(), [], [])
     assert p.rows() == 0
     rx.check_io(p, _desc(), None, None, None)  # an empty batch may pass no tensors
+
+
+def test_extend_kernel_choice_is_checked():
+    p = rx.Plan()
+    p.set_extend_kernel(rx.RX_EXTEND_PAIR)
+    p.set_extend_kernel(rx.RX_EXTEND_TILES)
+    for bad in (-1, 2, 7):
+        with pytest.raises(rx.RxError) as e:
+            p.set_extend_kernel(bad)
+        assert e.value.status == rx.RX_ERR_INVALID

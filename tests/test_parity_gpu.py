@@ -60,10 +60,12 @@ def stratified_decode_requests(d):
     return sorted(pick)
 
 
-def run_and_check(wl, cuda, sample=None, seed=0, decode_pick=None):
+def run_and_check(wl, cuda, sample=None, seed=0, decode_pick=None,
+                  extend_kernel=rx.RX_EXTEND_TILES):
     """Run every step of `wl` on the GPU and compare with the oracle: every row, or the rows of
-    `sample` random requests per batch, or (decode only) the requests decode_pick(batch) names."""
-    dw = DeviceWorkload(wl, cuda)
+    `sample` random requests per batch, or (decode only) the requests decode_pick(batch) names.
+    Extend plans run on `extend_kernel`."""
+    dw = DeviceWorkload(wl, cuda, extend_kernel=extend_kernel)
     rng = np.random.default_rng(seed)
     for i, st in enumerate(wl.steps):
         dw.run_step(i)
