@@ -267,11 +267,15 @@ def allreduce_max(pg, x, dev):
 
 
 def kernel_source_hash(name):
-    p = os.path.join(ROOT, "prefix_shared_kv_gb300", "csrc", name)
+    """sha1 of the kernel's source file followed by the planner's (rx_api.cpp: the order in which
+    items run decides what is re-read from DRAM)."""
+    h = hashlib.sha1()
     try:
-        return hashlib.sha1(open(p, "rb").read()).hexdigest()[:12]
+        for f in (name, "rx_api.cpp"):
+            h.update(open(os.path.join(ROOT, "prefix_shared_kv_gb300", "csrc", f), "rb").read())
     except OSError:
         return None
+    return h.hexdigest()[:12]
 
 
 def recorded_traffic(kernel_file, workload):
@@ -377,7 +381,7 @@ def main():
     roof["traffic"] = recorded_traffic(dom[1], wl.name)
     roof["traffic_source"] = (
         "recorded: dram__bytes_read.sum + dram__bytes_write.sum per launch from an earlier ncu "
-        "capture of this kernel source (hash) on this workload, profiles/dram_traffic.txt; not "
+        "capture of this kernel and planner source (hash) on this workload, profiles/dram_traffic.txt; not "
         "measured in this run" if roof["traffic"] is not None else
         "none: no ncu capture recorded for this kernel source and workload")
 

@@ -357,8 +357,8 @@ int launch_decode(const rx_kv_desc* d, const PlanHeader* h, const void* k_pool,
     return launch_attn_items(
         d, reinterpret_cast<const ExtItem*>(base + h->off_xitems),
         reinterpret_cast<const ExtRow*>(base + h->off_xrows),
-        reinterpret_cast<const ExtSeg*>(base + h->off_xsegs), h->n_xitems, k_pool, v_pool, q,
-        nullptr, nullptr, p.part_o, p.part_lse, p.status, st);
+        reinterpret_cast<const ExtSeg*>(base + h->off_xsegs), h->n_xitems, nullptr, 0, k_pool,
+        v_pool, q, nullptr, nullptr, p.part_o, p.part_lse, p.status, st);
   };
   if (h->n_xitems > 0 && h->n_items > 0) {
     // The tensor-core kernel takes whole SMs (one CTA fills an SM's shared memory), so it goes

@@ -71,6 +71,7 @@ struct ExtParams {
   float* part_o;    // non-null: write fp32 partial rows (decode shared-prefix units)
   float* part_lse;
   int n_items;
+  const int32_t* cta_begin;  // per-CTA item lists ([gridDim.x + 1] starts), or null: snake deal
   bool o32;         // o is 32-byte aligned: rows go out in 32-byte stores, else 16-byte ones
 };
 
@@ -154,13 +155,20 @@ __device__ __forceinline__ void tile_next(TileIter& c, const ExtSeg* segs, int n
   }
 }
 
-// The CTA's r-th item: the plan's list is dealt to the grid in snake order (round r holds items
-// r G .. r G + G - 1; CTA k takes the k-th of an even round and the (G - 1 - k)-th of an odd one),
-// so that a list sorted by falling cost gives every CTA a similar total.  -1 past the end.
-__device__ __forceinline__ int item_at(int r, int n_items) {
-  const int G = gridDim.x, k = blockIdx.x;
+// The CTA's r-th item, -1 past the end.  With per-CTA lists (extend plans) CTA k runs items
+// cta_begin[k] .. cta_begin[k + 1] - 1 in order.  Without (decode shared-prefix units) the list is
+// dealt to the grid in snake order (round r holds items r G .. r G + G - 1; CTA k takes the k-th
+// of an even round and the (G - 1 - k)-th of an odd one), so that a list sorted by falling cost
+// gives every CTA a similar total.
+__device__ __forceinline__ int item_at(const ExtParams& p, int r) {
+  const int k = blockIdx.x;
+  if (p.cta_begin) {
+    const int i = __ldg(&p.cta_begin[k]) + r;
+    return i < __ldg(&p.cta_begin[k + 1]) ? i : -1;
+  }
+  const int G = gridDim.x;
   const int64_t i = (int64_t)r * G + ((r & 1) ? G - 1 - k : k);
-  return i < n_items ? (int)i : -1;
+  return i < p.n_items ? (int)i : -1;
 }
 
 // Byte offset of 16-byte chunk c (0..15) of row r in a K-major tile stored as two 128-byte-
@@ -223,7 +231,7 @@ __device__ __forceinline__ void producer(const ExtParams& p, int w, uint32_t bas
   const uint32_t bar = base + kOffBar;
   uint32_t gs = 0;  // ring steps of the CTA's earlier items
   for (int ri = 0;; ++ri) {
-    const int idx = item_at(ri, p.n_items);
+    const int idx = item_at(p, ri);
     if (idx < 0) return;
     const ExtItem it = p.items[idx];
     const ExtSeg* segs = p.segs + it.seg_begin;
@@ -293,7 +301,7 @@ __device__ __forceinline__ void mma_issuer(const ExtParams& p, int x, uint32_t b
   // item), P steps of tile x, items of tile x
   uint32_t gs = 0, sv = 0, pb = 0, nq = 0;
   for (int ri = 0; ok; ++ri) {
-    const int idx = item_at(ri, p.n_items);
+    const int idx = item_at(p, ri);
     if (idx < 0) break;
     const ExtItem it = p.items[idx];
     const int ntiles = it.n_steps;
@@ -463,7 +471,7 @@ __device__ __forceinline__ bool has_tile(const ExtItem& it, int x) {
 // The CTA's first item from round *ri on that has tile x (-1: none); *ri is left at its round.
 __device__ __forceinline__ int first_item(const ExtParams& p, int x, int* ri) {
   for (;; ++*ri) {
-    const int idx = item_at(*ri, p.n_items);
+    const int idx = item_at(p, *ri);
     if (idx < 0 || has_tile(p.items[idx], x)) return idx;
   }
 }
@@ -659,7 +667,7 @@ __device__ __forceinline__ void softmax_role(const ExtParams& p, uint32_t base, 
     const ExtSeg* segs = p.segs + it.seg_begin;
     const int ntiles = it.n_steps;
     const bool two = it.n_tok[1] > 0;
-    const int nidx = item_at(ri + 1, p.n_items);
+    const int nidx = item_at(p, ri + 1);
     ExtItem nit = it;
     if (nidx >= 0) nit = p.items[nidx];
     RowQ nrow = row;
@@ -797,9 +805,10 @@ int make_pool_map(CUtensorMap* map, const void* pool, const rx_kv_desc* d) {
 }
 
 int launch_attn_items(const rx_kv_desc* d, const ExtItem* items, const ExtRow* rows,
-                      const ExtSeg* segs, int32_t n_items, const void* k_pool, const void* v_pool,
-                      const void* q, void* o, float* lse, float* part_o, float* part_lse,
-                      int32_t* status, void* stream) {
+                      const ExtSeg* segs, int32_t n_items, const int32_t* cta_begin,
+                      int32_t n_ctas, const void* k_pool, const void* v_pool, const void* q,
+                      void* o, float* lse, float* part_o, float* part_lse, int32_t* status,
+                      void* stream) {
   // kernel attributes belong to the current device: set once per device (bit d of the mask)
   static std::atomic<uint64_t> attr_set{0};
   int dev = 0;
@@ -845,12 +854,19 @@ int launch_attn_items(const rx_kv_desc* d, const ExtItem* items, const ExtRow* r
   if (e) return e;
   p.oob_row = (int32_t)(d->pool_size * d->num_kv_heads);
   p.n_items = n_items;
+  p.cta_begin = cta_begin;
   p.o32 = (reinterpret_cast<uintptr_t>(o) & 31u) == 0;
-  // one persistent CTA per SM (a CTA fills an SM's shared memory), at most one per item
-  int n_sm = 0;
-  const cudaError_t ce = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
-  if (ce != cudaSuccess) return (int)ce;
-  const int grid = n_items < n_sm ? n_items : n_sm;
+  // one persistent CTA per SM (a CTA fills an SM's shared memory), at most one per item; with
+  // per-CTA lists, one CTA per list (a plan made for a GPU with more SMs still runs: its extra
+  // CTAs start as others finish)
+  int grid = n_ctas;
+  if (!cta_begin) {
+    int n_sm = 0;
+    const cudaError_t ce = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
+    if (ce != cudaSuccess) return (int)ce;
+    grid = n_items < n_sm ? n_items : n_sm;
+  }
+  if (grid <= 0) return 0;
   extend_tc_kernel<<<grid, kThreads, kSmem, (cudaStream_t)stream>>>(p, k_map, v_map);
   return (int)cudaGetLastError();
 }
@@ -866,8 +882,9 @@ int launch_extend(const rx_kv_desc* d, const PlanHeader* h, const void* k_pool,
   if (h->ext_kernel == RX_EXTEND_PAIR)
     return launch_extend_pair(d, items, rows, segs, h->n_items, k_pool, v_pool, q, o, lse, status,
                               stream);
-  return launch_attn_items(d, items, rows, segs, h->n_items, k_pool, v_pool, q, o, lse, nullptr,
-                           nullptr, status, stream);
+  return launch_attn_items(d, items, rows, segs, h->n_items,
+                           reinterpret_cast<const int32_t*>(base + h->off_cta), h->n_ctas, k_pool,
+                           v_pool, q, o, lse, nullptr, nullptr, status, stream);
 }
 
 }  // namespace rx

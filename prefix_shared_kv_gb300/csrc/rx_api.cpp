@@ -11,6 +11,7 @@
 #include <limits>
 #include <memory>
 #include <numeric>
+#include <queue>
 #include <string>
 #include <unordered_map>
 #include <vector>
@@ -138,7 +139,21 @@ namespace {
 // units of a one-tile step (a step with both tiles takes about 7/6 of one).
 int32_t attn_steps(int64_t n) { return (int32_t)((n + kAttnKeys - 1) / kAttnKeys); }
 int64_t attn_cost(const ExtItem& it) { return (int64_t)it.n_steps * (it.n_tok[1] > 0 ? 7 : 6); }
-constexpr int64_t kCostClass = 4 * 7;  // four two-tile steps
+// What an item costs beyond its steps (its query tiles in, its rows out, the pipeline's fill),
+// in the same units: about two two-tile steps (the step time of the radix-mixed workload is
+// flat from 14 to 28 and 1-3 % longer at 0-7).
+constexpr int64_t kItemCost = 14;
+
+// SMs of the calling thread's current GPU, the number of per-CTA lists an extend plan for the
+// one-SM kernel makes; a GB300's 152 where no GPU can be asked (plans are host work).
+int32_t plan_sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess &&
+      cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && n > 0)
+    return n;
+  (void)cudaGetLastError();
+  return 152;
+}
 // On the SM-pair kernel an item takes steps of kPairKeys keys per segment and costs its steps
 // whether or not it has a second tile (the other CTA gathers and multiplies anyway).
 int32_t pair_steps(int64_t n) { return (int32_t)((n + kPairKeys - 1) / kPairKeys); }
@@ -791,8 +806,8 @@ rx_status rx_extend_plan_tree(rx_plan* plan, const rx_kv_desc* desc, int32_t bat
   }
 
   // Launch order: largest unit first (longest-processing-time first across units); inside a
-  // unit, KV head outer and pairs inner, so the tiles that read the same prefix K/V of one head
-  // run in the same wave and hit in L2.
+  // unit, KV head outer and pairs inner (for the one-SM kernel then sorted, stably, costliest
+  // first), so the tiles that read the same prefix K/V run in the same wave and hit in L2.
   std::vector<size_t> order(units.size());
   std::iota(order.begin(), order.end(), 0);
   std::stable_sort(order.begin(), order.end(),
@@ -804,7 +819,8 @@ rx_status rx_extend_plan_tree(rx_plan* plan, const rx_kv_desc* desc, int32_t bat
     for (const Pair& pr : pairs[k])
       for (int i = 0; i < pr.n_seg; ++i)
         key_reads += (int64_t)(segs[pr.seg_begin + i].k_end - segs[pr.seg_begin + i].k_begin) * hkv;
-  for (size_t k : order)
+  for (size_t k : order) {
+    const size_t unit_first = items.size();
     for (int h = 0; h < hkv; ++h)
       for (const Pair& pr : pairs[k]) {
         const Tile& ta = units[k].tiles[pr.a];
@@ -823,16 +839,49 @@ rx_status rx_extend_plan_tree(rx_plan* plan, const rx_kv_desc* desc, int32_t bat
         }
         items.push_back(it);
       }
-  // The attention kernel deals the list to its CTAs (clusters) in rounds (snake order): sorted
-  // by falling cost, every CTA gets a similar total.  The sort is by cost classes (four two-tile
-  // steps, or two pair steps) and keeps the planned order (a unit's KV heads and tiles together)
-  // inside a class, so items that read the same prefix still tend to run at the same time and
-  // share it in L2.
-  std::stable_sort(items.begin(), items.end(), [&](const ExtItem& a, const ExtItem& b) {
-    if (pair_kernel) return a.n_steps / kPairCostClass > b.n_steps / kPairCostClass;
-    return attn_cost(a) / kCostClass > attn_cost(b) / kCostClass;
-  });
+    // inside a unit the costliest items first (a long causal tile reads all the keys before it)
+    if (!pair_kernel)
+      std::stable_sort(items.begin() + unit_first, items.end(),
+                       [](const ExtItem& a, const ExtItem& b) {
+                         return attn_cost(a) > attn_cost(b);
+                       });
+  }
   if (items.size() > (size_t)INT32_MAX) return fail(RX_ERR_RANGE, "plan too large");
+  std::vector<int32_t> cta_begin;
+  if (pair_kernel) {
+    // The pair kernel deals the list to its clusters in rounds (snake order): sorted by falling
+    // cost, every cluster gets a similar total.  The sort is by cost classes two steps wide and
+    // keeps the planned order (a unit's KV heads and tiles together) inside a class.
+    std::stable_sort(items.begin(), items.end(), [](const ExtItem& a, const ExtItem& b) {
+      return a.n_steps / kPairCostClass > b.n_steps / kPairCostClass;
+    });
+  } else if (!items.empty()) {
+    // One list per CTA, made by list scheduling in the planned order (largest unit first; in a
+    // unit, costliest item first): each item goes to the CTA whose list ends first under
+    // the cost model.  A CTA runs its list in order, so items next to each other in the planned
+    // order start at about the same time on different SMs -- the tiles of one unit read its
+    // prefix and its causal keys while they are in L2 -- and the lists end at about the same
+    // time.  The table is stored CTA by CTA.
+    const int32_t G = (int32_t)std::min<int64_t>(plan_sm_count(), (int64_t)items.size());
+    using Slot = std::pair<int64_t, int32_t>;  // (end of the list, CTA)
+    std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> free_at;
+    for (int32_t k = 0; k < G; ++k) free_at.push({0, k});
+    std::vector<std::vector<int32_t>> lists(G);
+    for (size_t i = 0; i < items.size(); ++i) {
+      const Slot s = free_at.top();
+      free_at.pop();
+      lists[s.second].push_back((int32_t)i);
+      free_at.push({s.first + attn_cost(items[i]) + kItemCost, s.second});
+    }
+    std::vector<ExtItem> by_cta;
+    by_cta.reserve(items.size());
+    cta_begin.push_back(0);
+    for (const auto& l : lists) {
+      for (int32_t i : l) by_cta.push_back(items[i]);
+      cta_begin.push_back((int32_t)by_cta.size());
+    }
+    items.swap(by_cta);
+  }
 
   PlanHeader h;
   std::memset(&h, 0, sizeof h);
@@ -848,6 +897,8 @@ rx_status rx_extend_plan_tree(rx_plan* plan, const rx_kv_desc* desc, int32_t bat
   h.off_items = off; off = align256(off + items.size() * sizeof(ExtItem));
   h.off_rows = off; off = align256(off + rows.size() * sizeof(ExtRow));
   h.off_segs = off; off = align256(off + segs.size() * sizeof(ExtSeg));
+  h.off_cta = off; off = align256(off + cta_begin.size() * sizeof(int32_t));
+  h.n_ctas = cta_begin.empty() ? 0 : (int32_t)cta_begin.size() - 1;
   h.off_merge_idx = h.off_merge = h.off_part_o = h.off_part_lse = off;
   h.total_bytes = off;
   plan->blob.assign(off, 0);
@@ -855,6 +906,7 @@ rx_status rx_extend_plan_tree(rx_plan* plan, const rx_kv_desc* desc, int32_t bat
   put(plan->blob, h.off_items, items);
   put(plan->blob, h.off_rows, rows);
   put(plan->blob, h.off_segs, segs);
+  put(plan->blob, h.off_cta, cta_begin);
   plan->ws_bytes = off;
   plan->key_reads = key_reads;
   plan->kind = 1;

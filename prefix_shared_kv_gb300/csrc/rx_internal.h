@@ -105,7 +105,11 @@ struct PlanHeader {
   int64_t off_xitems, off_xrows, off_xsegs;
   int32_t n_xitems;
   int32_t ext_kernel;    // extend plans: RX_EXTEND_TILES or RX_EXTEND_PAIR
-  int64_t pad[15];
+  // extend plans on the one-SM kernel: per-CTA item lists, int32 [n_ctas + 1] starts into the
+  // item table (which is stored CTA by CTA); n_ctas = 0 when the items are dealt in snake order
+  int64_t off_cta;
+  int32_t n_ctas, pad32;
+  int64_t pad[13];
 };
 static_assert(sizeof(PlanHeader) == 256, "header is 256 bytes");
 
@@ -138,11 +142,14 @@ int launch_extend_pair(const rx_kv_desc* d, const ExtItem* items, const ExtRow* 
 int make_pool_map(CUtensorMap* map, const void* pool, const rx_kv_desc* d);
 // The tensor-core attention kernel over `n_items` items of tables in device memory; with
 // part_o != nullptr every tile writes fp32 partial rows (normalised O, base-2 LSE) instead of o /
-// lse.  `status` is the plan's device status word.
+// lse.  `status` is the plan's device status word.  With `cta_begin` (device, [n_ctas + 1]) the
+// grid is n_ctas CTAs and CTA k runs items cta_begin[k] .. cta_begin[k + 1] - 1; with null the
+// items are dealt to one CTA per SM in snake order.
 int launch_attn_items(const rx_kv_desc* d, const ExtItem* items, const ExtRow* rows,
-                      const ExtSeg* segs, int32_t n_items, const void* k_pool, const void* v_pool,
-                      const void* q, void* o, float* lse, float* part_o, float* part_lse,
-                      int32_t* status, void* stream);
+                      const ExtSeg* segs, int32_t n_items, const int32_t* cta_begin,
+                      int32_t n_ctas, const void* k_pool, const void* v_pool, const void* q,
+                      void* o, float* lse, float* part_o, float* part_lse, int32_t* status,
+                      void* stream);
 
 // The plan's second stream for a decode call on the current device (created on first use); all
 // NULL when the plan's calls launch a single kernel.
