@@ -30,12 +30,13 @@
 //                memory), move it only when the row's max exceeds it by more than 2^8 (then O is
 //                rescaled), hand it on, write P = 2^(s - m) as bf16 over the upper half of the S
 //                buffer.  Each warpgroup keeps its own sum; at the end they merge (O, LSE).
-//                Warpgroup 0 copies the query rows in.  exp2_poly2 can take part of the
-//                exponentials onto the FMA pipe (kPolyPairs).
+//                exp2_poly2 can take part of the exponentials onto the FMA pipe (kPolyPairs).
 //   warps 8-10   K producers (steps t = 0, 1, 2 mod 3), warps 11-13 V producers: gather rows by
 //                slot with TMA tile::gather4 (four pool rows of 64 columns per instruction, 128-
 //                byte swizzle by the copy engine) into 5-stage rings; a stage lands on the CTA's
-//                own barrier (bytes counted).
+//                own barrier (bytes counted).  The V warp that takes an item's first ring step
+//                first copies the item's query rows in (cp.async), once the previous item's
+//                copy is done and its last S MMA has read the old rows.
 //   warp 14      even CTA: the MMA issuer (one thread); odd CTA: the relay, which forwards each
 //                of its landed stages to the even CTA's barrier for the peer half.
 //   warp 15      tensor-memory allocation for the pair (one warp in each CTA); in the even CTA
@@ -43,8 +44,8 @@
 //                publishes its progress in shared memory, since a barrier operation after a
 //                commit holds the issuing thread until the tensor pipe has taken the MMAs before
 //                it (measured: 40-75 ns per wait, most of a step's slack).
-// The issuer keeps S two steps ahead: per step t it issues O += P(t) V(t), then S(t+3) into the
-// buffer P(t) sat in (one thread's MMAs execute in order).  Its commits arrive on the barriers of
+// With three S buffers the issuer keeps S up to three steps ahead of PV: per step t it issues
+// O += P(t) V(t), then S(t+3) into the buffer P(t) sat in (one thread's MMAs execute in order).  Its commits arrive on the barriers of
 // both CTAs at once (multicast).  Steps, S steps, P steps and items are running counts across
 // the CTA's items, so the pipelines never drain between items.
 // Every mbarrier wait is bounded (globaltimer); a timeout records RX_ERR_TIMEOUT in the workspace
