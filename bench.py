@@ -393,7 +393,7 @@ def main():
         per_workload = {}
         del dw
         torch.cuda.empty_cache()
-        for name in ("extend", "decode", "gqa-decode"):
+        for name in ("extend", "decode", "gqa-decode", "paged"):
             if name == args.workload:
                 continue
             # structure-only build (slots, lengths, new tokens' KV, queries drawn on the host as

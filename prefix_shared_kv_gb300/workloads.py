@@ -325,7 +325,8 @@ def decode_workload(seed: int, num_q_heads: int, num_kv_heads: int, *, n_groups:
 
 
 def paged_workload(seed: int, num_q_heads: int, num_kv_heads: int, *, page: int, prefix: int,
-                   n_req: int, ext_lo: int, ext_hi: int, name: str = "paged") -> Workload:
+                   n_req: int, ext_lo: int, ext_hi: int, name: str = "paged",
+                   values: bool = True) -> Workload:
     """Block-granular pool (prefix-caching comparison page: vLLM keeps KV in blocks and reuses only
     whole blocks).  n_req requests share a cached `prefix` of which only floor(prefix / page) *
     page tokens -- whole pages -- are reused; each request recomputes the rest of the prefix and
@@ -336,7 +337,7 @@ def paged_workload(seed: int, num_q_heads: int, num_kv_heads: int, *, page: int,
     ext = rng.integers(ext_lo, ext_hi + 1, size=n_req)
     need_pages = shared // page + int(sum((prefix - shared + e + 1 + page - 1) // page + 1 for e in ext))
     P = max(4096, 1 << int(np.ceil(np.log2(need_pages * page * 1.25 + 1))))
-    b = Builder(rng, num_q_heads, num_kv_heads, P, page=page)
+    b = Builder(rng, num_q_heads, num_kv_heads, P, page=page, values=values)
     pre = b.cached(shared) if shared > 0 else None
     cached_seqs = [(pre.tokens.copy(), pre.slots.copy())] if pre is not None else []
     new_runs, rows, pl, el, toks, cur_runs = [], [], [], [], [], []
@@ -516,6 +517,14 @@ def llama7b_extend(seed: int = 1002, values: bool = True) -> Workload:
                            values=values)
 
 
+def llama7b_paged(seed: int = 1007, values: bool = True) -> Workload:
+    """The extend workload's shape on a block-granular pool: 32/32 heads, pages of 16 slots in
+    random page order; 64 requests on a 2000-token prefix (all of it whole pages, so all reused),
+    each extending U[40,200] new tokens in pages of its own; then one decode step."""
+    return paged_workload(seed, 32, 32, page=16, prefix=2000, n_req=64, ext_lo=40, ext_hi=200,
+                          name="llama7b-paged16-64-p2000", values=values)
+
+
 def llama7b_decode_hf(seed: int = 1003, values: bool = True) -> Workload:
     """32/32 heads; 16 groups x 16 requests on a 2000-token prefix; distinct U[100,500]."""
     return decode_workload(seed, 32, 32, n_groups=16, members=16, prefix=2000, dist_lo=100,
@@ -596,4 +605,5 @@ NAMED = {
     "radix-mixed": radix_mixed,
     "radix-mixed-1level": lambda values=True: radix_mixed(tree=False, values=values),
     "chunked-prefill": llama3_chunked_prefill,
+    "paged": llama7b_paged,
 }

@@ -502,6 +502,20 @@ def test_block_granular_pool(cuda, hq, hkv, prefix):
     run_and_check(wl, cuda)
 
 
+def test_block_granular_pool_odd_pages_and_mid_page_prefix(cuda):
+    """Pages of 24 slots (a page boundary inside a kernel step, pages not aligned to 16 slots);
+    pages of 16 with a declared shared prefix of 985 while the rows share 992 (the members' own
+    keys start mid-page)."""
+    run_and_check(W.paged_workload(61, 8, 2, page=24, prefix=1000, n_req=5, ext_lo=1,
+                                   ext_hi=150), cuda)
+    wl = W.paged_workload(62, 16, 4, page=16, prefix=1000, n_req=6, ext_lo=1, ext_hi=150)
+    for st in wl.steps:
+        for b in (st.extend, st.decode):
+            if b is not None:
+                b.group_prefix_len = np.asarray([985], dtype=b.group_prefix_len.dtype)
+    run_and_check(wl, cuda)
+
+
 # ---------------------------------------------------------------------------------------------
 # Full-size workloads in the benchmark's configuration.  Every extend and decode row of the
 # extend, radix-mixed (tree and one-level) and chunked-prefill workloads; for the two decode
@@ -510,7 +524,7 @@ def test_block_granular_pool(cuda, hq, hkv, prefix):
 # ---------------------------------------------------------------------------------------------
 
 @pytest.mark.parametrize("name", ["extend", "radix-mixed", "radix-mixed-1level",
-                                  "chunked-prefill"])
+                                  "chunked-prefill", "paged"])
 def test_full_size_workloads_every_row(cuda, name):
     run_and_check(W.NAMED[name](), cuda)
 

@@ -147,3 +147,25 @@ def test_chunked_prefill():
         if i:
             assert (own == wl.steps[0].decode.seq_len - 1024 - 1).all()
     assert distinct_tokens_have_distinct_slots(wl)
+
+
+def test_paged():
+    """The block-granular configuration: every key position p of a request sits in slot
+    page * 16 + p % 16 of one of its pages, so every whole page is a run of 16 consecutive
+    slots."""
+    assert W.NAMED["paged"] is W.llama7b_paged
+    a = W.paged_workload(5, 4, 2, page=16, prefix=90, n_req=3, ext_lo=1, ext_hi=40)
+    b = W.paged_workload(5, 4, 2, page=16, prefix=90, n_req=3, ext_lo=1, ext_hi=40,
+                         values=False)
+    assert b.k_pool.shape[0] == 0 and np.array_equal(a.req_to_token, b.req_to_token)
+    wl = W.NAMED["paged"](values=False)
+    e = wl.steps[0].extend
+    assert (wl.num_q_heads, wl.num_kv_heads) == (32, 32) and len(e.req_idx) == 64
+    assert (e.prefix_len == 2000).all() and e.extend_len.min() >= 40 and e.extend_len.max() <= 200
+    assert rows_share(wl.req_to_token, list(e.req_idx), 2000)
+    assert distinct_tokens_have_distinct_slots(wl)
+    for r, p, x in zip(e.req_idx, e.prefix_len, e.extend_len):
+        s = wl.req_to_token[r, :p + x].astype(np.int64)
+        assert (s % 16 == np.arange(p + x) % 16).all()          # position p in slot 16 k + p % 16
+        full = (p + x) // 16 * 16
+        assert (np.diff(s[:full].reshape(-1, 16), axis=1) == 1).all()  # whole pages are runs
