@@ -360,11 +360,15 @@ int launch_decode(const rx_kv_desc* d, const PlanHeader* h, const void* k_pool,
         reinterpret_cast<const ExtSeg*>(base + h->off_xsegs), h->n_xitems, nullptr, 0, k_pool,
         v_pool, q, nullptr, nullptr, p.part_o, p.part_lse, p.status, st);
   };
+  cudaStream_t merge_stream = s;
   if (h->n_xitems > 0 && h->n_items > 0) {
     // The tensor-core kernel takes whole SMs (one CTA fills an SM's shared memory), so it goes
     // first, on the caller's stream with nothing to wait for; the mma.sync units follow on the
     // plan's second stream (fork and join through events, so the pair also works under stream
     // capture) and fill the other SMs.  Each kernel's last wave would otherwise leave SMs idle.
+    // The mma.sync units end last, so the merge is queued right behind them on the second stream
+    // (after a wait for the tensor-core kernel, long done by then) and the caller's stream joins
+    // after the merge: the merge starts as the units end instead of after a join and a launch.
     if (!aux || !aux->stream || !aux->fork || !aux->join) return (int)cudaErrorInvalidValue;
     cudaStream_t a = (cudaStream_t)aux->stream;
     cudaError_t ce = cudaEventRecord((cudaEvent_t)aux->fork, s);
@@ -375,9 +379,11 @@ int launch_decode(const rx_kv_desc* d, const PlanHeader* h, const void* k_pool,
     if (ce != cudaSuccess) return (int)ce;
     decode_partial_kernel<<<h->n_items, kThreads, kDecSmemBytes, a>>>(p);
     ce = cudaGetLastError();
-    if (ce == cudaSuccess) ce = cudaEventRecord((cudaEvent_t)aux->join, a);
-    if (ce == cudaSuccess) ce = cudaStreamWaitEvent(s, (cudaEvent_t)aux->join, 0);
+    // the fork event again, now behind the tensor-core kernel (a wait takes the record before it)
+    if (ce == cudaSuccess) ce = cudaEventRecord((cudaEvent_t)aux->fork, s);
+    if (ce == cudaSuccess) ce = cudaStreamWaitEvent(a, (cudaEvent_t)aux->fork, 0);
     if (ce != cudaSuccess) return (int)ce;
+    merge_stream = a;
   } else if (h->n_xitems > 0) {
     const int e = run_x(s);
     if (e) return e;
@@ -387,12 +393,17 @@ int launch_decode(const rx_kv_desc* d, const PlanHeader* h, const void* k_pool,
   if (h->batch > 0) {
     const int64_t tasks = (int64_t)h->batch * p.hq;
     decode_merge_kernel<<<(unsigned)((tasks + kMergeWarps - 1) / kMergeWarps), 32 * kMergeWarps, 0,
-                          s>>>(
+                          merge_stream>>>(
         p.part_o, p.part_lse, reinterpret_cast<const int32_t*>(base + h->off_merge_idx),
         reinterpret_cast<const DecMergeRef*>(base + h->off_merge), h->batch, p.hq, p.gq,
         static_cast<__nv_bfloat16*>(o), lse);
   }
-  return (int)cudaGetLastError();
+  cudaError_t ce = cudaGetLastError();
+  if (ce == cudaSuccess && merge_stream != s) {
+    ce = cudaEventRecord((cudaEvent_t)aux->join, merge_stream);
+    if (ce == cudaSuccess) ce = cudaStreamWaitEvent(s, (cudaEvent_t)aux->join, 0);
+  }
+  return (int)ce;
 }
 
 }  // namespace rx
