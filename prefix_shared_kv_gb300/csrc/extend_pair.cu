@@ -92,15 +92,15 @@ static_assert(kWarpAlloc == 15, "sixteen warps: two softmax warpgroups, two othe
 constexpr int kRegsLaunch = 65536 / kThreads;  // 128
 constexpr int kRegsSoftmax = 200, kRegsOther = 56;
 static_assert(kRegsSoftmax * 256 + kRegsOther * 256 <= kRegsLaunch * kThreads, "register split");
-constexpr int kStages = 5;
+constexpr int kStages = 4;  // (with two Q buffers, five stages would not fit in shared memory)
 static_assert(kStages >= kPW, "a producer could run two phases ahead");
 constexpr int kQHalf = 128 * 128;      // 64 columns of the 128 query rows: 16 KiB
 constexpr int kQTile = 2 * kQHalf;
 constexpr int kKHalf = 64 * 128;       // 64 columns of the CTA's 64 keys of a step: 8 KiB
 constexpr int kKTile = 2 * kKHalf;     // 16 KiB
 constexpr int kVTile = kN * 128;       // the CTA's 64 columns of the step's 128 V rows: 16 KiB
-constexpr int kOffQ = 0;
-constexpr int kOffK = kQTile;
+constexpr int kOffQ = 0;               // two Q buffers: item i uses buffer i % 2
+constexpr int kOffK = 2 * kQTile;
 constexpr int kOffV = kOffK + kStages * kKTile;
 constexpr int kOffBar = kOffV + kStages * kVTile;
 // Barriers, at the same offsets in both CTAs (each waiter is at most one phase behind):
@@ -112,10 +112,12 @@ constexpr int kOffBar = kOffV + kStages * kVTile;
 //   PF[b]          even CTA only: P(t) of both CTAs in buffer b = t % 3 (one arrival per warp of
 //                  step t's softmax warpgroup, either CTA; one barrier per buffer, since the
 //                  softmax may run up to two steps ahead of the issuer)
-//   QF             the CTA's query rows of the item are in its Q buffer (the Q loader)
-//   QP             even CTA only: the odd CTA's query rows landed (the relay's arrival)
-//   QE             every S MMA of the item complete: the Q buffer may take the next item's rows
-//                  (multicast commit after the item's last S)
+//   QF[q]          the CTA's query rows of an item are in Q buffer q (the Q loader; phase = the
+//                  buffer's uses)
+//   QP[q]          even CTA only: the odd CTA's query rows in buffer q landed (the relay)
+//   QE[q]          every S MMA of the item in buffer q complete: the buffer may take the rows of
+//                  the item after next (multicast commit after the item's last S).  One barrier
+//                  per buffer, so that a loader that runs late never tests a phase two ahead
 //   OD             every MMA of the item complete: O is final (multicast commit)
 //   DR             even CTA only: every MMA complete, at the end (tensor memory may be released)
 //   ML[i]          the CTA's two softmax warpgroups have stored their (max, sum) of the row for
@@ -131,10 +133,10 @@ enum {
   B_VF = B_KF + kStages,
   B_SF = B_VF + kStages,  // + b
   B_PF = B_SF + 3,        // + b
-  B_QF = B_PF + 3,
-  B_QP = B_QF + 1,
-  B_QE = B_QP + 1,
-  B_OD = B_QE + 1,
+  B_QF = B_PF + 3,        // + Q buffer
+  B_QP = B_QF + 2,        // + Q buffer
+  B_QE = B_QP + 2,        // + Q buffer
+  B_OD = B_QE + 2,
   B_DR = B_OD + 1,
   B_ML = B_DR + 1,        // + item parity
   B_MR = B_ML + 2,        // + step parity
@@ -249,20 +251,22 @@ struct Slot4 {
   int v[4];
 };
 
-// The CTA's query rows of item `it` (the nq-th with steps), copied by one warp into the Q buffer
-// (tile_off layout: two 64-column halves, 128-byte swizzle; rows past the tile's as zeros) with
-// cp.async once every S MMA of the item before has completed (QE); then the warp makes its writes
-// visible to the tensor core (proxy fence) and lane 0 arrives on QF.  Lane l copies tile rows
+// The CTA's query rows of item `it` (the nq-th with steps), copied by one warp into Q buffer
+// nq % 2 (tile_off layout: two 64-column halves, 128-byte swizzle; rows past the tile's as zeros)
+// with cp.async once every S MMA of item nq - 2, the buffer's previous user, has completed
+// (QE[nq % 2]), so the rows land while item nq - 1 still runs; then the warp makes its writes
+// visible to the tensor core (proxy fence) and lane 0 arrives on QF[nq % 2].  Lane l copies tile rows
 // l, l + 32, l + 64, l + 96.  (A TMA copy would queue behind the ring's prefetched gathers:
 // measured 5 us from the item's last S to its rows landing.)  Returns false when a wait gave up.
 __device__ __forceinline__ bool load_q_rows(const PairParams& p, const ExtItem& it, uint32_t rank,
                                             uint32_t base, uint32_t nq, volatile int* filled_q,
                                             volatile int* abort) {
   const int lane = threadIdx.x & 31;
-  const uint32_t bar = base + kOffBar, qb = base + kOffQ;
+  const uint32_t q = nq & 1;
+  const uint32_t bar = base + kOffBar, qb = base + kOffQ + q * kQTile;
   // Another V warp copies the previous item's rows and may still be waiting for its own turn:
-  // this warp runs up to a ring ahead of the issuer, and testing QE's parity before the copy of
-  // item nq - 1 has passed QE's phase nq - 2 would pass on that earlier phase.
+  // this warp runs up to a ring ahead of the issuer, and testing QE[q]'s parity before the copy
+  // of item nq - 2 has passed its previous phase would pass on that earlier phase.
   bool ok = true;
   if (nq > 0) {
     const uint64_t t0 = pair::globaltimer();
@@ -276,7 +280,8 @@ __device__ __forceinline__ bool load_q_rows(const PairParams& p, const ExtItem& 
       }
       __nanosleep(64);
     }
-    ok = ok && pair::wait(bar + 8 * B_QE, (nq - 1) & 1, abort, p.status, kWaitNs);
+    if (nq > 1)
+      ok = ok && pair::wait(bar + 8 * (B_QE + q), ((nq - 2) >> 1) & 1, abort, p.status, kWaitNs);
   }
   if (__any_sync(0xffffffffu, !ok)) return false;
   const int n_tok = rank ? it.n_tok[1] : it.n_tok[0];
@@ -297,7 +302,7 @@ __device__ __forceinline__ bool load_q_rows(const PairParams& p, const ExtItem& 
   tc::fence_proxy_async();
   __syncwarp();
   if (lane == 0) {
-    tc::mbar_arrive(bar + 8 * B_QF);
+    tc::mbar_arrive(bar + 8 * (B_QF + q));
     *filled_q = (int)nq + 1;
   }
   return true;
@@ -394,7 +399,8 @@ __device__ __forceinline__ void gate_role(const PairParams& p, uint32_t base,
     if (idx < 0) return;
     const int ntiles = p.items[idx].n_steps;
     if (ntiles == 0) continue;
-    if (!wait(B_QF, nq & 1) || !wait(B_QP, nq & 1)) return;  // both CTAs' query rows
+    // both CTAs' query rows, in Q buffer nq % 2
+    if (!wait(B_QF + (nq & 1), (nq >> 1) & 1) || !wait(B_QP + (nq & 1), (nq >> 1) & 1)) return;
     pair::st_release(gate, ++passed);
     for (int t = 0; t < kSBuf && t < ntiles; ++t) {
       if (!landed(B_KL, B_KP, gs + t)) return;
@@ -423,7 +429,7 @@ __device__ __forceinline__ void mma_issuer(const PairParams& p, uint32_t base, u
   constexpr uint32_t idS = tc::idesc_bf16(256, kN, false, false);
   constexpr uint32_t idO = tc::idesc_bf16(256, 128, false, true);
   const uint32_t bar = base + kOffBar, gate = base + kOffGate;
-  const uint64_t qdesc = tc::desc_sw128(base + kOffQ, 16, 1024);
+  const uint64_t qdesc0 = tc::desc_sw128(base + kOffQ, 16, 1024);
   const uint64_t kdesc0 = tc::desc_sw128(base + kOffK, 16, 1024);
   const uint64_t vdesc0 = tc::desc_sw128(base + kOffV, kVTile, 1024);
   const uint32_t d_o = tmem + kColO;
@@ -449,6 +455,7 @@ __device__ __forceinline__ void mma_issuer(const PairParams& p, uint32_t base, u
     if (idx < 0) break;
     const int ntiles = p.items[idx].n_steps;
     if (ntiles == 0) continue;  // (plans hold none; every role skips them alike)
+    const uint64_t qdesc = qdesc0 + (((nq & 1) * kQTile) >> 4);  // the item's Q buffer
     auto qk = [&](int t) {  // S(t) = Q K(t)^T into buffer (sv + t) % 3
       const uint64_t kd = kdesc0 + ((((gs + t) % kStages) * kKTile) >> 4);
       const uint32_t d_s = tmem + col_s_of((sv + t) % kSBuf);
@@ -472,7 +479,7 @@ __device__ __forceinline__ void mma_issuer(const PairParams& p, uint32_t base, u
         qk(t);
         pair::commit_mc(bar + 8 * (B_SF + (sv + t) % kSBuf), kBoth);
         pair::commit_mc(bar + 8 * (B_KF + (gs + t) % kStages), kBoth);
-        if (t == ntiles - 1) pair::commit_mc(bar + 8 * B_QE, kBoth);  // the item's last S
+        if (t == ntiles - 1) pair::commit_mc(bar + 8 * (B_QE + (nq & 1)), kBoth);  // last S
       } else {
         pair::commit_mc(bar + 8 * (B_SF + (sv + t) % kSBuf), kBoth);  // step without an MMA
       }
@@ -487,7 +494,7 @@ __device__ __forceinline__ void mma_issuer(const PairParams& p, uint32_t base, u
       pair::commit_mc(bar + 8 * (B_VF + gt % kStages), kBoth);
       pair::commit_mc(bar + 8 * (B_SF + (sv + t) % kSBuf), kBoth);  // also after the last steps
       if (more) pair::commit_mc(bar + 8 * (B_KF + gt3 % kStages), kBoth);
-      if (more && t + kSBuf == ntiles - 1) pair::commit_mc(bar + 8 * B_QE, kBoth);
+      if (more && t + kSBuf == ntiles - 1) pair::commit_mc(bar + 8 * (B_QE + (nq & 1)), kBoth);
     }
     if (!ok) break;
     pair::commit_mc(bar + 8 * B_OD, kBoth);
@@ -520,9 +527,9 @@ __device__ __forceinline__ void relay(const PairParams& p, uint32_t base, volati
     const int ntiles = p.items[idx].n_steps;
     if (ntiles == 0) continue;
     // the item's query rows first: the issuer waits for them before its first S
-    ok = ok && pair::wait(bar + 8 * B_QF, nq & 1, abort, p.status, kWaitNs);
+    ok = ok && pair::wait(bar + 8 * (B_QF + (nq & 1)), (nq >> 1) & 1, abort, p.status, kWaitNs);
     if (!ok) return;
-    pair::arrive_remote(pair::map_to(bar + 8 * B_QP, 0));
+    pair::arrive_remote(pair::map_to(bar + 8 * (B_QP + (nq & 1)), 0));
     ++nq;
     for (int t = 0; t < kSBuf && t < ntiles; ++t)
       if (!fwd(B_KL, B_KP, gs + t)) return;
@@ -851,9 +858,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       tc::mbar_init(bar + 8 * (B_SF + b), 1);
       tc::mbar_init(bar + 8 * (B_PF + b), 8);  // the four warps of a step's warpgroup, both CTAs
     }
-    tc::mbar_init(bar + 8 * B_QF, 1);
-    tc::mbar_init(bar + 8 * B_QP, 1);
-    tc::mbar_init(bar + 8 * B_QE, 1);
+    for (int q = 0; q < 2; ++q) {
+      tc::mbar_init(bar + 8 * (B_QF + q), 1);
+      tc::mbar_init(bar + 8 * (B_QP + q), 1);
+      tc::mbar_init(bar + 8 * (B_QE + q), 1);
+    }
     for (int b = 0; b < 2; ++b) {
       tc::mbar_init(bar + 8 * (B_ML + b), 256);
       tc::mbar_init(bar + 8 * (B_MR + b), 128);
@@ -899,11 +908,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   __syncthreads();
   if (threadIdx.x < 2 * kStages + 1) {
     const int f = filled[threadIdx.x];
+    const bool is_q = threadIdx.x == 2 * kStages;  // f = Q loads: the last went to buffer (f-1) % 2
     const int b = threadIdx.x < kStages       ? B_KL + threadIdx.x
                   : threadIdx.x < 2 * kStages ? B_VL + (threadIdx.x - kStages)
-                                              : B_QF;
+                                              : B_QF + ((f - 1) & 1);
+    const uint32_t parity = is_q ? (uint32_t)((f - 1) >> 1) & 1 : (uint32_t)(f - 1) & 1;
     int no_abort = 0;
-    if (f > 0) pair::wait(bar + 8 * b, (uint32_t)(f - 1) & 1, &no_abort, p.status, kWaitNs);
+    if (f > 0) pair::wait(bar + 8 * b, parity, &no_abort, p.status, kWaitNs);
   }
   tc::fence_before();
   __syncthreads();

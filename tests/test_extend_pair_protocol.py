@@ -76,9 +76,12 @@ def simulate(items, stages, producer_warps, seed, p_rescale=0.3, nbuf=3, q_in_or
     for b in range(nbuf):
         make((0, "PF", b), 2)
     for c in range(2):
-        make((c, "QF"), 1)  # the CTA's Q loader (expect_tx) + its gathers' bytes
-        make((c, "QE"), 1)  # commit after an item's last S
-    make((0, "QP"), 1)      # the relay: the odd CTA's query rows landed
+        for qb in range(2):
+            make((c, "QF", qb), 1)  # the CTA's query rows of an item in Q buffer qb
+        for qb in range(2):
+            make((c, "QE", qb), 1)  # commit after the last S of an item that used Q buffer qb
+    for qb in range(2):
+        make((0, "QP", qb), 1)  # the relay: the odd CTA's query rows in buffer qb landed
     make((0, "DR"), 1)
 
     tma = {0: [], 1: []}                      # gathers in flight per CTA
@@ -88,8 +91,8 @@ def simulate(items, stages, producer_warps, seed, p_rescale=0.3, nbuf=3, q_in_or
     reading = {(c, op): [set() for _ in range(stages)] for c in range(2) for op in "KV"}
     sbuf = {(c, b): None for c in range(2) for b in range(nbuf)}  # ("S", id) or ("P", id)
     p_used = set()
-    qbuf = {0: None, 1: None}
-    qk_pending = [0]
+    qbuf = {(c, qb): None for c in range(2) for qb in range(2)}  # item whose rows a buffer holds
+    qk_pending = [0, 0]  # S MMAs issued, not yet executed, per Q buffer they read
     o_state = {0: None, 1: None}              # (item, last PV step executed)
     o_read = {0: set(), 1: set()}
     m_slot = {(c, b): None for c in range(2) for b in range(2)}  # (item, step) of a stored max
@@ -137,9 +140,9 @@ def simulate(items, stages, producer_warps, seed, p_rescale=0.3, nbuf=3, q_in_or
             bars[(0, op + "P", st)].arrive()
         for i, n in enumerate(work):
             gs = steps_before[i]
-            while not ready((1, "QF"), i):
+            while not ready((1, "QF", i & 1), i >> 1):
                 yield
-            bars[(0, "QP")].arrive()
+            bars[(0, "QP", i & 1)].arrive()
             for t in range(min(nbuf, n)):
                 yield from fwd("K", gs + t)
             for t in range(n):
@@ -159,14 +162,14 @@ def simulate(items, stages, producer_warps, seed, p_rescale=0.3, nbuf=3, q_in_or
 
         for i, n in enumerate(work):
             gs = steps_before[i]
-            while not ready((0, "QF"), nq):
+            while not ready((0, "QF", nq & 1), nq >> 1):
                 yield
-            while not ready((0, "QP"), nq):
+            while not ready((0, "QP", nq & 1), nq >> 1):
                 yield
 
             def qk(t):
                 pipe.append(("QK", (sv + t) % nbuf, (i, t), (gs + t) % stages, gs + t))
-                qk_pending[0] += 1
+                qk_pending[i & 1] += 1
                 for c in range(2):
                     reading[(c, "K")][(gs + t) % stages].add((i, t))
 
@@ -182,7 +185,7 @@ def simulate(items, stages, producer_warps, seed, p_rescale=0.3, nbuf=3, q_in_or
                     pipe.append(("SF", (sv + t) % nbuf))
                     pipe.append(("KF", (gs + t) % stages))
                     if t == n - 1:
-                        pipe.append(("QE",))
+                        pipe.append(("QE", i & 1))
                 else:
                     pipe.append(("SF", (sv + t) % nbuf))  # a step without an MMA
             for t in range(n):
@@ -201,7 +204,7 @@ def simulate(items, stages, producer_warps, seed, p_rescale=0.3, nbuf=3, q_in_or
                 if more:
                     pipe.append(("KF", g2 % stages))
                 if more and t + nbuf == n - 1:
-                    pipe.append(("QE",))
+                    pipe.append(("QE", i & 1))
                 yield
             pipe.append(("OD",))
             sv += n + nbuf
@@ -214,19 +217,22 @@ def simulate(items, stages, producer_warps, seed, p_rescale=0.3, nbuf=3, q_in_or
     q_loaded = {0: 0, 1: 0}  # the CTA's count of items whose query rows were copied in
 
     def load_q(c, i):
-        """The CTA's query rows of item i, once item i-1's were copied in (so that the wait on
-        QE is for its next phase) and item i-1's S MMAs are done."""
+        """The CTA's query rows of item i into Q buffer i % 2, once item i-1's were copied in (so
+        that the wait on QE is for its next phase) and the S MMAs of item i-2, the buffer's
+        previous item, are done."""
+        qb = i & 1
         if i > 0:
             while q_in_order and q_loaded[c] < i:
                 yield
-            while not ready((c, "QE"), i - 1):
+        if i > 1:
+            while not ready((c, "QE", qb), (i - 2) >> 1):
                 yield
-            if qk_pending[0]:
-                raise RuntimeError(f"Q of CTA {c} overwritten with an S MMA pending")
-        qbuf[c] = ("loading", i)
+            if qk_pending[qb]:
+                raise RuntimeError(f"Q buffer {qb} of CTA {c} overwritten with an S MMA pending")
+        qbuf[(c, qb)] = ("loading", i)
         yield
-        qbuf[c] = i
-        bars[(c, "QF")].arrive()
+        qbuf[(c, qb)] = i
+        bars[(c, "QF", qb)].arrive()
         q_loaded[c] = i + 1
         yield
 
@@ -293,8 +299,9 @@ def simulate(items, stages, producer_warps, seed, p_rescale=0.3, nbuf=3, q_in_or
                 if ring[(c, "K")][st] != g or landed[(c, "K")][st] != g:
                     raise RuntimeError(f"S MMA {sid} reads K stage {st} of CTA {c}: "
                                        f"{ring[(c, 'K')][st]}")
-                if qbuf[c] != sid[0]:
-                    raise RuntimeError(f"S MMA {sid} reads Q of CTA {c} = {qbuf[c]}")
+                if qbuf[(c, sid[0] & 1)] != sid[0]:
+                    raise RuntimeError(f"S MMA {sid} reads Q of CTA {c} = "
+                                       f"{qbuf[(c, sid[0] & 1)]}")
                 cur = sbuf[(c, b)]
                 if cur is not None and cur[0] == "S":
                     raise RuntimeError(f"S MMA {sid} overwrites unread {cur} in CTA {c}")
@@ -302,7 +309,7 @@ def simulate(items, stages, producer_warps, seed, p_rescale=0.3, nbuf=3, q_in_or
                     raise RuntimeError(f"S MMA {sid} overwrites unused {cur} in CTA {c}")
                 sbuf[(c, b)] = ("S", sid)
                 reading[(c, "K")][st].discard(sid)
-            qk_pending[0] -= 1
+            qk_pending[op[2][0] & 1] -= 1
         elif op[0] == "PV":
             _, b, pid, st, g, t = op
             for c in range(2):
@@ -319,7 +326,7 @@ def simulate(items, stages, producer_warps, seed, p_rescale=0.3, nbuf=3, q_in_or
             bars[(0, "DR")].arrive()
         elif op[0] == "QE":
             for c in range(2):
-                bars[(c, "QE")].arrive()
+                bars[(c, "QE", op[1])].arrive()
         else:  # a commit multicast to both CTAs
             for c in range(2):
                 bars[(c,) + op].arrive()
@@ -333,9 +340,7 @@ def simulate(items, stages, producer_warps, seed, p_rescale=0.3, nbuf=3, q_in_or
             c = rnd.randrange(2)
             if tma[c]:
                 key, k, op, st, g = tma[c].pop(rnd.randrange(len(tma[c])))
-                if op == "Q":
-                    qbuf[c] = g
-                elif ring[(c, op)][st] == g and not any(e[2] == op and e[3] == st and e[4] == g
+                if ring[(c, op)][st] == g and not any(e[2] == op and e[3] == st and e[4] == g
                                                         for e in tma[c]):
                     landed[(c, op)][st] = g
                 bars[key].complete_tx(k)
@@ -360,7 +365,7 @@ def simulate(items, stages, producer_warps, seed, p_rescale=0.3, nbuf=3, q_in_or
             raise RuntimeError(f"CTA {c} wrote out items {sorted(o_read[c])}")
 
 
-STAGES, PRODUCER_WARPS, S_BUFFERS = 5, 3, 3  # the kernel's kStages, kPW and kSBuf
+STAGES, PRODUCER_WARPS, S_BUFFERS = 4, 3, 3  # the kernel's kStages, kPW and kSBuf
 
 
 def test_random_item_lists():
