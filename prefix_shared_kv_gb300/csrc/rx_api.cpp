@@ -136,13 +136,13 @@ struct rx_plan {
 namespace {
 
 // Steps of the tensor-core attention kernel over a segment of n keys, and an item's cost in
-// units of a one-tile step (a step with both tiles takes about 7/6 of one).
+// fourteenths of a two-tile step.  The weights are a least-squares fit of the per-CTA times of
+// the extend, radix-mixed (tree and one-level), chunked-prefill and paged workloads (globaltimer
+// at each CTA's entry and exit, 760 CTAs): a two-tile step 1.03 µs, a one-tile step 0.81 µs, and
+// 4.9 µs per item beyond its steps (its query tiles in, its rows out, the pipelines' refill).
 int32_t attn_steps(int64_t n) { return (int32_t)((n + kAttnKeys - 1) / kAttnKeys); }
-int64_t attn_cost(const ExtItem& it) { return (int64_t)it.n_steps * (it.n_tok[1] > 0 ? 7 : 6); }
-// What an item costs beyond its steps (its query tiles in, its rows out, the pipeline's fill),
-// in the same units: about two two-tile steps (the step time of the radix-mixed workload is
-// flat from 14 to 28 and 1-3 % longer at 0-7).
-constexpr int64_t kItemCost = 14;
+int64_t attn_cost(const ExtItem& it) { return (int64_t)it.n_steps * (it.n_tok[1] > 0 ? 14 : 11); }
+constexpr int64_t kItemCost = 66;
 
 // SMs of the calling thread's current GPU, the number of per-CTA lists an extend plan for the
 // one-SM kernel makes; a GB300's 152 where no GPU can be asked (plans are host work).
@@ -867,11 +867,40 @@ rx_status rx_extend_plan_tree(rx_plan* plan, const rx_kv_desc* desc, int32_t bat
     std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> free_at;
     for (int32_t k = 0; k < G; ++k) free_at.push({0, k});
     std::vector<std::vector<int32_t>> lists(G);
+    auto cost_of = [&](int32_t i) { return attn_cost(items[i]) + kItemCost; };
     for (size_t i = 0; i < items.size(); ++i) {
       const Slot s = free_at.top();
       free_at.pop();
       lists[s.second].push_back((int32_t)i);
-      free_at.push({s.first + attn_cost(items[i]) + kItemCost, s.second});
+      free_at.push({s.first + cost_of((int32_t)i), s.second});
+    }
+    // The lists' ends are left up to one item apart, and the last units' items are large (a
+    // branch's 1,700-key tile, a long causal tile).  Balance them: while it lowers the larger of
+    // the two, move from the longest list to the shortest the item whose cost best splits their
+    // gap (appended at the end, so the longest list's other items only start earlier).
+    std::vector<int64_t> load(G, 0);
+    for (int32_t k = 0; k < G; ++k)
+      for (int32_t i : lists[k]) load[k] += cost_of(i);
+    for (int32_t round = 0; round < 8 * G; ++round) {
+      const int32_t hi = (int32_t)(std::max_element(load.begin(), load.end()) - load.begin());
+      const int32_t lo = (int32_t)(std::min_element(load.begin(), load.end()) - load.begin());
+      const int64_t gap = load[hi] - load[lo];
+      int64_t best_gain = 0;
+      size_t best = 0;
+      for (size_t j = 0; j < lists[hi].size(); ++j) {
+        const int64_t c = cost_of(lists[hi][j]);
+        const int64_t gain = std::min(c, gap - c);  // the longer list shortens by this much
+        if (c < gap && gain > best_gain) {
+          best_gain = gain;
+          best = j;
+        }
+      }
+      if (best_gain <= 0) break;
+      const int32_t i = lists[hi][best];
+      lists[hi].erase(lists[hi].begin() + (std::ptrdiff_t)best);
+      lists[lo].push_back(i);
+      load[hi] -= cost_of(i);
+      load[lo] += cost_of(i);
     }
     std::vector<ExtItem> by_cta;
     by_cta.reserve(items.size());
