@@ -147,6 +147,9 @@ rx_status rx_plan_upload(const rx_plan* plan, void* workspace, size_t workspace_
  * be < 2^31.  batch == 0 builds a plan with no work: the attention call then enqueues nothing and
  * may be given NULL tensors.  o needs 16-byte alignment; at 32-byte alignment rows are written in
  * 32-byte pieces.
+ * On the default kernel (rx_plan_set_extend_kernel) the plan deals its work items into one list
+ * per SM of the calling thread's current GPU (152 where no GPU is visible); the attention call
+ * launches one CTA per list, so the plan runs on any GPU, at its best on one with as many SMs.
  * ------------------------------------------------------------------------------------------- */
 rx_status rx_extend_plan(rx_plan* plan, const rx_kv_desc* desc, int32_t batch,
                          const int32_t* req_idx, const int32_t* prefix_len,
